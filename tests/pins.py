@@ -1,0 +1,385 @@
+"""Pins for the CPU oracle: each checks the oracle against something other than
+itself -- published known-answer vectors, closed forms, numpy/scipy library
+routines, brute force on tiny inputs, and distributional facts the
+FlashSampling pages rest on (the Gumbel-max identity, argmax decomposition
+over partitions, the group log-mass merge).
+
+Every pin is a function ``pin_x(o)`` of an ``oracle.Oracle`` that raises
+AssertionError on failure, so the same pins run against the real oracle
+(test_oracle_pins.py) and against copies with a planted mistake
+(test_oracle_mutants.py).
+"""
+from __future__ import annotations
+
+import math
+import os
+
+import numpy as np
+import scipy.special
+import scipy.stats
+
+from oracle import EULER_GAMMA, GUMBEL_VAR
+from oracle.merge import (chi_square_gof, group_gumbel_max, lse_merge,
+                          online_merge, partition_argmax)
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+P_MIN = 1e-3  # significance level of every goodness-of-fit pin
+
+
+# ---- helpers ----------------------------------------------------------------
+def bf16_to_f64(bits):
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def f32_to_bf16_bits(x):
+    """Round-to-nearest-even float32 -> bf16 bit patterns (input generation)."""
+    u = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return r.astype(np.uint16)
+
+
+def make_problem(B, d, V, seed, scale=1.0):
+    rng = np.random.default_rng(seed)
+    H = f32_to_bf16_bits(rng.standard_normal((B, d)).astype(np.float32))
+    W = f32_to_bf16_bits((rng.standard_normal((V, d)) * (2.0 / math.sqrt(d)) * scale).astype(np.float32))
+    return H, W
+
+
+def ref_logits(H, W):
+    """The library fp64 matmul of the same bf16 values."""
+    return bf16_to_f64(H) @ bf16_to_f64(W).T
+
+
+def draws(o, H, W, n, T, seed=0, mask=None, row=0, start=0):
+    """n samples of one row at offsets start..start+n-1."""
+    B = H.shape[0]
+    temp = np.full(B, T, dtype=np.float32)
+    out = np.empty(n, dtype=np.int64)
+    for i in range(n):
+        out[i] = o.sample(H, W, temperature=temp, mask=mask, seed=seed,
+                          offset=start + i, rows=[row])["idx"][0]
+    return out
+
+
+def pack_mask(allow):
+    """bool [B, V] -> uint32 [B, ceil(V/32)] allow-bits."""
+    B, V = allow.shape
+    n = (V + 31) // 32
+    pad = np.zeros((B, n * 32), dtype=bool)
+    pad[:, :V] = allow
+    w = (pad.reshape(B, n, 32).astype(np.uint64) << np.arange(32, dtype=np.uint64)).sum(-1)
+    return w.astype(np.uint32)
+
+
+# ---- Philox and the noise transform -------------------------------------
+def pin_philox_kat(o):
+    """Philox4x32-10 reproduces the published known-answer vectors."""
+    path = os.path.join(GOLDEN, "philox4x32_10_kat.txt")
+    n = 0
+    for line in open(path):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        lhs, rhs = line.split("->")
+        ins = [int(x, 16) for x in lhs.split()]
+        want = [int(x, 16) for x in rhs.split()]
+        got = [int(x) for x in o.philox(ins[:4], ins[4:6])]
+        assert got == want, f"philox({lhs.strip()}) = {[hex(g) for g in got]}"
+        n += 1
+    assert n == 3
+
+
+def pin_uniform_map(o):
+    """u = ((w >> 9) + 1/2) 2^-23: endpoints, bit use, open interval."""
+    assert o.uniform(0) == 2.0 ** -24
+    assert o.uniform(0xFFFFFFFF) == 1.0 - 2.0 ** -24
+    assert o.uniform(0x1FF) == 2.0 ** -24            # low 9 bits unused
+    assert o.uniform(0x200) == 3.0 * 2.0 ** -24
+    assert o.uniform(0x80000000) == 0.5 + 2.0 ** -24
+    rng = np.random.default_rng(7)
+    ws = rng.integers(0, 2 ** 32, size=2000, dtype=np.uint64)
+    us = np.array([o.uniform(int(w)) for w in ws])
+    assert np.all((us > 0) & (us < 1))
+    # exact in fp32
+    assert np.all(us.astype(np.float32).astype(np.float64) == us)
+
+
+def pin_gumbel_closed_forms(o):
+    """g(u) = -log(-log u): g(e^-1) = 0, and g inverts the Gumbel CDF."""
+    assert abs(o.gumbel(math.exp(-1.0))) < 1e-15
+    for x in (-2.0, -0.5, 0.0, 0.3, 1.0, 4.0, 9.0):
+        u = math.exp(-math.exp(-x))
+        assert abs(o.gumbel(u) - x) < 1e-9 * max(1.0, abs(x)) + 1e-12, x
+    # monotone increasing
+    us = np.linspace(0.001, 0.999, 101)
+    gs = np.array([o.gumbel(u) for u in us])
+    assert np.all(np.diff(gs) > 0)
+
+
+def pin_noise_distribution(o):
+    """Noise over a (row, vocab) grid is Gumbel(0,1): KS test, mean gamma,
+    variance pi^2/6."""
+    g = o.noise_grid(0, 64, 0, 4096, seed=12345, offset=7).ravel()
+    n = g.size
+    ks = scipy.stats.kstest(g, scipy.stats.gumbel_r.cdf)
+    assert ks.pvalue > P_MIN, ks
+    assert abs(g.mean() - EULER_GAMMA) < 5 * math.sqrt(GUMBEL_VAR / n)
+    assert abs(g.var() - GUMBEL_VAR) < 0.03
+
+
+def pin_noise_independence(o):
+    """No two of (vocab index, row, offset, seed words, offset words) share
+    noise: the streams that differ in exactly one of them are uncorrelated."""
+    base = o.noise_grid(0, 8, 0, 4096, seed=99, offset=5)
+
+    def corr(a, b):
+        return float(np.corrcoef(a.ravel(), b.ravel())[0, 1])
+
+    lim = 0.02
+    # adjacent vocab indices (inside one Philox block of four and across)
+    for shift in (1, 2, 3, 4):
+        c = corr(base[:, :-shift], base[:, shift:])
+        assert abs(c) < lim, ("vocab", shift, c)
+    assert abs(corr(base[:-1], base[1:])) < lim                       # rows
+    other = [
+        o.noise_grid(0, 8, 0, 4096, seed=99, offset=6),               # offset
+        o.noise_grid(0, 8, 0, 4096, seed=99, offset=5 + (1 << 32)),   # offset hi word
+        o.noise_grid(0, 8, 0, 4096, seed=100, offset=5),              # seed
+        o.noise_grid(0, 8, 0, 4096, seed=99 + (1 << 32), offset=5),   # seed hi word
+    ]
+    for k, x in enumerate(other):
+        c = corr(base, x)
+        assert abs(c) < lim, (k, c)
+    # per-row seeds: row b takes seeds[b]
+    seeds = np.array([99, 99 + (1 << 40), 7, 99], dtype=np.uint64)
+    ps = o.noise_grid(0, 4, 0, 256, seeds=seeds, offset=5)
+    assert np.array_equal(ps[0], base[0, :256])
+    assert np.array_equal(ps[3], base[3, :256])
+    assert abs(corr(ps[1], base[1, :256])) < 0.25
+
+
+# ---- logits, greedy, tiles ------------------------------------------------
+def pin_logits_match_numpy(o):
+    """fp64 logits equal numpy's fp64 matmul of the same bf16 values."""
+    H, W = make_problem(5, 72, 300, seed=1)
+    got = o.logits(H, W)
+    want = ref_logits(H, W)
+    assert np.allclose(got, want, rtol=1e-12, atol=1e-12)
+    s = o.sample(H, W, temperature=np.zeros(5, np.float32), want_logits=True)
+    assert np.allclose(s["logits"], want, rtol=1e-12, atol=1e-12)
+
+
+def pin_greedy_is_argmax(o):
+    """T = 0 (and T < 0, NaN, inf) is greedy: numpy.argmax of the fp64
+    logits, lowest index on exact ties, with per-tile maxima of the logits."""
+    B, d, V = 6, 32, 700
+    H, W = make_problem(B, d, V, seed=2)
+    W[513] = W[2]            # exact duplicates -> exact logit ties,
+    W[640] = W[129]          # in another tile and in the same tile
+    W[130] = W[129]
+    L = ref_logits(H, W)
+    for T in (0.0, -1.0, float("nan"), float("inf")):
+        r = o.sample(H, W, temperature=np.full(B, T, np.float32), seed=3, offset=4)
+        assert np.array_equal(r["idx"], np.argmax(L, axis=1)), T
+        for t in range((V + 127) // 128):
+            blk = L[:, t * 128:(t + 1) * 128]
+            assert np.array_equal(r["tile_idx"][:, t], t * 128 + np.argmax(blk, axis=1))
+            assert np.allclose(r["tile_max"][:, t], blk.max(axis=1), rtol=1e-12, atol=1e-12)
+            assert np.allclose(r["tile_lse"][:, t], blk.max(axis=1), rtol=1e-12, atol=1e-12)
+    # tie rule, forced: make row 0's best logit tie across tiles
+    H1 = H[:1].copy()
+    W2 = W.copy()
+    best = int(np.argmax(L[0]))
+    W2[699] = W2[best]
+    W2[best + 1 if best + 1 < 699 else best - 1] = W2[best]
+    r = o.sample(H1, W2, temperature=np.zeros(1, np.float32))
+    L2 = ref_logits(H1, W2)[0]
+    assert r["idx"][0] == np.argmax(L2)
+    for t in range((V + 127) // 128):   # the tie inside best's tile included
+        assert r["tile_idx"][0, t] == t * 128 + np.argmax(L2[t * 128:(t + 1) * 128])
+
+
+def pin_tile_outputs(o):
+    """Per-tile (max, argmax, log-sum-exp, top-2 gap) against brute force
+    over the scores, with library logsumexp over the numpy logits; a ragged
+    last tile, a masked-out tile and masked entries included."""
+    B, d, V, T = 3, 24, 1000, float(np.float32(0.7))
+    H, W = make_problem(B, d, V, seed=3)
+    allow = np.ones((B, V), dtype=bool)
+    rng = np.random.default_rng(0)
+    allow &= rng.random((B, V)) > 0.1
+    allow[1, 256:384] = False            # a fully masked tile
+    mask = pack_mask(allow)
+    r = o.sample(H, W, temperature=np.full(B, T, np.float32), mask=mask,
+                 seed=5, offset=11, want_scores=True, want_logits=True)
+    L = ref_logits(H, W)
+    assert np.allclose(r["logits"], L, rtol=1e-12, atol=1e-12)
+    S = r["scores"]
+    assert np.all(np.isneginf(S[~allow]))
+    assert np.all(np.isfinite(S[allow]))
+    g = o.noise_grid(0, B, 0, V, seed=5, offset=11)
+    assert np.allclose(S[allow], (L / T + g)[allow], rtol=1e-12, atol=1e-12)
+    nt = (V + 127) // 128
+    for b in range(B):
+        for t in range(nt):
+            lo, hi = t * 128, min(V, t * 128 + 128)
+            s = S[b, lo:hi]
+            ok = allow[b, lo:hi]
+            if not ok.any():
+                assert r["tile_idx"][b, t] == -1
+                assert np.isneginf(r["tile_max"][b, t]) and np.isneginf(r["tile_lse"][b, t])
+                continue
+            assert r["tile_idx"][b, t] == lo + int(np.argmax(s))
+            assert r["tile_max"][b, t] == s.max()
+            top2 = np.sort(s[ok])[-2:]
+            assert np.isclose(r["tile_gap"][b, t], top2[1] - top2[0], rtol=1e-12, atol=1e-12)
+            lse = scipy.special.logsumexp(L[b, lo:hi][ok] / T)
+            assert np.isclose(r["tile_lse"][b, t], lse, rtol=1e-12, atol=1e-12)
+        assert r["idx"][b] == int(np.argmax(S[b]))
+        top2 = np.sort(S[b][allow[b]])[-2:]
+        assert np.isclose(r["gap"][b], top2[1] - top2[0], rtol=1e-12, atol=1e-12)
+    # large logits: the log-sum-exp must not overflow
+    Hb, Wb = make_problem(1, 16, 256, seed=4, scale=300.0)
+    rb = o.sample(Hb, Wb, temperature=np.full(1, 0.5, np.float32))
+    Lb = ref_logits(Hb, Wb)
+    for t in range(2):
+        want = scipy.special.logsumexp(Lb[0, t * 128:(t + 1) * 128] / 0.5)
+        assert np.isfinite(rb["tile_lse"][0, t]) and np.isclose(rb["tile_lse"][0, t], want, rtol=1e-12)
+
+
+def pin_fully_masked_row(o):
+    """A row with every entry masked samples -1; other rows are unaffected."""
+    H, W = make_problem(2, 16, 300, seed=6)
+    allow = np.ones((2, 300), dtype=bool)
+    allow[0] = False
+    r = o.sample(H, W, mask=pack_mask(allow), seed=1)
+    r2 = o.sample(H, W, seed=1)
+    assert r["idx"][0] == -1 and np.all(r["tile_idx"][0] == -1)
+    assert r["idx"][1] == r2["idx"][1]
+
+
+def pin_partition_invariance(o):
+    """The argmax decomposes over partitions: tiles of any width and any
+    grouping of tiles give the flat argmax, bit for bit."""
+    B, d, V = 4, 16, 777
+    H, W = make_problem(B, d, V, seed=7)
+    T = np.full(B, 0.9, np.float32)
+    flat = o.sample(H, W, temperature=T, seed=8, offset=3, tile=V, want_scores=True)
+    assert np.array_equal(flat["idx"], np.argmax(flat["scores"], axis=1))
+    rng = np.random.default_rng(1)
+    for tile in (1, 7, 64, 128, 500):
+        r = o.sample(H, W, temperature=T, seed=8, offset=3, tile=tile)
+        nt = r["tile_max"].shape[1]
+        assert np.array_equal(r["idx"], flat["idx"])
+        for b in range(B):
+            for _ in range(4):
+                cuts = np.sort(rng.choice(np.arange(1, nt), size=min(3, nt - 1), replace=False)) if nt > 1 else []
+                bounds = [0, *cuts.tolist(), nt] if nt > 1 else [0, nt]
+                i, m = partition_argmax(r["tile_max"][b], r["tile_idx"][b], bounds)
+                assert i == flat["idx"][b] and m == flat["scores"][b].max()
+
+
+def pin_lse_merge(o):
+    """log-sum-exp of the tile log-masses is the whole row's log-mass."""
+    B, d, V, T = 3, 16, 1000, float(np.float32(1.3))
+    H, W = make_problem(B, d, V, seed=9)
+    r = o.sample(H, W, temperature=np.full(B, T, np.float32))
+    L = ref_logits(H, W)
+    for b in range(B):
+        assert np.isclose(lse_merge(r["tile_lse"][b]),
+                          scipy.special.logsumexp(L[b] / T), rtol=1e-12, atol=1e-12)
+
+
+# ---- distribution ------------------------------------------------------------
+def pin_chi_square_softmax(o):
+    """Seeded draws follow softmax(l / T) exactly (Pearson chi-square)."""
+    for (V, d, T, n, seed) in ((16, 16, 0.7, 20000, 11), (64, 8, 1.0, 20000, 12)):
+        H, W = make_problem(1, d, V, seed=seed)
+        p = scipy.special.softmax(ref_logits(H, W)[0] / T)
+        idx = draws(o, H, W, n, T, seed=seed)
+        counts = np.bincount(idx, minlength=V)
+        stat, dof, pval = chi_square_gof(counts, p)
+        assert pval > P_MIN, (V, T, stat, dof, pval)
+
+
+def pin_two_way_closed_form(o):
+    """V = 2: P(token 0) = sigmoid((l0 - l1) / T) (binomial z-test)."""
+    H, W = make_problem(1, 8, 2, seed=13)
+    L = ref_logits(H, W)[0]
+    T, n = 0.6, 20000
+    p0 = 1.0 / (1.0 + math.exp(-(L[0] - L[1]) / T))
+    k = int(np.sum(draws(o, H, W, n, T, seed=21) == 0))
+    z = (k - n * p0) / math.sqrt(n * p0 * (1 - p0))
+    assert abs(z) < 4.5, (k, n * p0, z)
+
+
+def pin_max_stability(o):
+    """Max-stability: m_t - L_t ~ Gumbel(0,1) for every tile, over draws."""
+    H, W = make_problem(1, 16, 256, seed=14)
+    T = np.full(1, 0.8, np.float32)
+    n = 6000
+    diffs = []
+    for off in range(n):
+        r = o.sample(H, W, temperature=T, seed=77, offset=off)
+        diffs.append(r["tile_max"][0] - r["tile_lse"][0])
+    diffs = np.asarray(diffs)
+    for t in range(diffs.shape[1]):
+        x = diffs[:, t]
+        assert abs(x.mean() - EULER_GAMMA) < 4.5 * math.sqrt(GUMBEL_VAR / n), (t, x.mean())
+        ks = scipy.stats.kstest(x, scipy.stats.gumbel_r.cdf)
+        assert ks.pvalue > P_MIN, (t, ks)
+
+
+def pin_group_merges(o):
+    """Group-Gumbel-Max and the online binary merge over 4 vocabulary groups,
+    fed the groups' own samples and log-masses, follow softmax(l / T)."""
+    V, d, T, n = 64, 8, 0.9, 12000
+    H, W = make_problem(1, d, V, seed=15)
+    p = scipy.special.softmax(ref_logits(H, W)[0] / T)
+    rng = np.random.default_rng(2)
+    temp = np.full(1, T, np.float32)
+    hier, online = [], []
+    for off in range(n):
+        r = o.sample(H, W, temperature=temp, seed=31, offset=off, tile=16)
+        z, L = r["tile_idx"][0], r["tile_lse"][0]
+        hier.append(group_gumbel_max(z, L, rng.random(4)))
+        online.append(online_merge(z, L, rng.random(4))[0])
+    for name, idx in (("group", hier), ("online", online)):
+        counts = np.bincount(np.asarray(idx), minlength=V)
+        stat, dof, pval = chi_square_gof(counts, p)
+        assert pval > P_MIN, (name, stat, dof, pval)
+
+
+def pin_masked_distribution(o):
+    """With a mask, draws follow softmax over the allowed tokens only."""
+    V, d, T, n = 40, 8, 1.0, 15000
+    H, W = make_problem(1, d, V, seed=16)
+    allow = np.ones((1, V), dtype=bool)
+    allow[0, [0, 3, 17, 18, 33]] = False
+    Lg = ref_logits(H, W)[0] / T
+    Lg[~allow[0]] = -np.inf
+    p = scipy.special.softmax(Lg)
+    idx = draws(o, H, W, n, T, seed=41, mask=pack_mask(allow))
+    assert np.all(allow[0, idx])
+    stat, dof, pval = chi_square_gof(np.bincount(idx, minlength=V)[allow[0]], p[allow[0]])
+    assert pval > P_MIN, (stat, dof, pval)
+
+
+ALL_PINS = [
+    pin_philox_kat,
+    pin_uniform_map,
+    pin_gumbel_closed_forms,
+    pin_logits_match_numpy,
+    pin_greedy_is_argmax,
+    pin_tile_outputs,
+    pin_fully_masked_row,
+    pin_partition_invariance,
+    pin_lse_merge,
+    pin_noise_distribution,
+    pin_noise_independence,
+    pin_two_way_closed_form,
+    pin_chi_square_softmax,
+    pin_masked_distribution,
+    pin_max_stability,
+    pin_group_merges,
+]
