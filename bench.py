@@ -1,0 +1,494 @@
+#!/usr/bin/env python
+"""Benchmark of the fused LM-head + exact Gumbel-max sampler (one GPU per rank).
+
+A step is one fs_sample call (stage 1 + stage 2) over one batch of the
+synthetic Qwen3-8B-shaped head (d=4096, V=151936): per-row temperatures
+U[0.5,1.5] with 10% greedy rows, per-row seeds, the Philox offset advancing by
+one per step.  W (1.24 GB) exceeds L2, so every step streams it from HBM.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle on a
+bounded sample of the same workload instead.  Under torchrun with N > 1 ranks,
+each rank runs an independent replica (the batch path has no exchange step).
+"""
+from __future__ import annotations
+
+import argparse
+import datetime
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "µs/call and % of HBM/tensor roofline, fused LM-head+sample, d=4096 V=151936"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="qwen3-8b")
+    ap.add_argument("--batch", type=int, default=64)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--sweep-steps", type=int, default=200)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="CPU budget of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def algorithmic(B, d, V, *, mask=False, lse=False, seeds=True, temperature=True):
+    """Bytes and flops one stage-1 launch must move / do: W and H once, the
+    per-row parameters, the mask bits, and the per-tile outputs."""
+    nt = (V + 127) // 128
+    by = V * d * 2 + B * d * 2 + B * nt * 8
+    by += B * 4 if temperature else 0
+    by += B * 8 if seeds else 0
+    by += B * ((V + 31) // 32) * 4 if mask else 0
+    by += B * nt * 4 if lse else 0
+    return by, 2.0 * B * V * d
+
+
+def roofline(B, d, V, us, peaks, traffic=None, **kw):
+    by, fl = algorithmic(B, d, V, **kw)
+    t_hbm = by / (peaks["hbm_gbs"] * 1e9)
+    t_tc = fl / (peaks["bf16_tflops"] * 1e12)
+    if t_hbm >= t_tc:
+        ach = by / (us * 1e-6) / 1e9
+        out = {"bound": "hbm", "achieved": round(ach, 1), "peak": peaks["hbm_gbs"],
+               "unit": "GB/s", "frac": round(ach / peaks["hbm_gbs"], 4)}
+    else:
+        ach = fl / (us * 1e-6) / 1e12
+        out = {"bound": "tensor", "achieved": round(ach, 1), "peak": peaks["bf16_tflops"],
+               "unit": "TFLOP/s", "frac": round(ach / peaks["bf16_tflops"], 4)}
+    out["traffic"] = traffic
+    out["algorithmic_bytes"] = by
+    out["algorithmic_flops"] = fl
+    out["peak_source"] = peaks["source"]
+    return out
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in ("lm_head_gumbel_gb300/csrc/fs_sample.cu", "lm_head_gumbel_gb300/csrc/fs_ptx.cuh",
+                "lm_head_gumbel_gb300/csrc/fs_noise.cuh"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload, B):
+    """DRAM bytes per stage-1 launch from the committed ncu summary, if it was
+    taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "stage1_traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        if rec.get("source_sha") != kernel_source_hash():
+            return None
+        ent = rec.get("launches", {}).get(f"{workload}/B={B}")
+        return None if ent is None else int(ent["dram_bytes_per_launch"])
+    except (OSError, ValueError, KeyError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons, every 100 ms."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+
+    def start(self):
+        self.fd, self.path = tempfile.mkstemp(suffix=".csv")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fd, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return []
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        os.close(self.fd)
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    rows.append({"t": ts, "sm": float(parts[1]), "sm_max": float(parts[2]),
+                                 "power": parts[3], "active": parts[4],
+                                 "hw_slowdown": parts[5], "hw_thermal_slowdown": parts[6],
+                                 "sw_thermal_slowdown": parts[7], "sw_power_cap": parts[8]})
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        return rows
+
+    @staticmethod
+    def summarize(rows, t0, t1):
+        inside = [r for r in rows if t0 <= r["t"] <= t1]
+        window = "timed region"
+        if not inside:
+            inside, window = rows, "measurement phase"
+        if not inside:
+            return None
+        reasons = sorted({k for r in inside for k in ("hw_slowdown", "hw_thermal_slowdown",
+                                                      "sw_thermal_slowdown", "sw_power_cap")
+                          if r[k].lower() == "active"})
+        return {"sm_mhz": statistics.median(r["sm"] for r in inside),
+                "sm_max_mhz": max(r["sm_max"] for r in inside), "reasons": reasons,
+                "samples": len(inside), "window": window}
+
+
+# ---------------------------------------------------------------------------
+def dist_init(backend):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def make_inputs(wl_name, B, device):
+    import torch
+    from lm_head_gumbel_gb300 import workloads as wl
+    w = wl.WORKLOADS[wl_name]
+    W = wl.make_weights(w.d, w.V, seed=77, device=device, outlier_frac=w.outlier_frac)
+    H = wl.make_hidden(B, w.d, seed=2000 + B, device=device)
+    T = wl.make_temperature(w, B, seed=3000 + B, device=device)
+    seeds = wl.make_seeds(B, base=4000 + B, device=device) if w.per_row_seeds else None
+    mask = wl.make_mask(B, w.V, w.mask_frac, seed=5000 + B, device=device) if w.mask_frac else None
+    return w, {"H": H, "W": W, "temperature": T, "seeds": seeds, "vocab_mask": mask}
+
+
+def time_calls(fn, steps, stream):
+    import torch
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for k in range(steps):
+        fn(k)
+    e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1)  # ms
+
+
+def run_ours(args):
+    import torch
+    import lm_head_gumbel_gb300 as fs
+
+    world, rank, local = dist_init("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    fs.load_library()
+    peaks = load_peaks()
+    B = args.batch
+    w, inp = make_inputs(args.workload, B, dev)
+    d, V = w.d, w.V
+    nt = fs.fs_num_tiles(V)
+    stream = torch.cuda.current_stream(dev)
+    out = torch.empty(B, dtype=torch.int64, device=dev)
+    ws = torch.empty(fs.fs_workspace_size(B, V), dtype=torch.uint8, device=dev)
+    tmax = torch.empty((B, nt), dtype=torch.float32, device=dev)
+    tidx = torch.empty((B, nt), dtype=torch.int32, device=dev)
+
+    def call(k, base=0):
+        fs.fs_sample(inp["H"], inp["W"], temperature=inp["temperature"], seeds=inp["seeds"],
+                     vocab_mask=inp["vocab_mask"], offset=base + k, out_idx=out, workspace=ws,
+                     stream=stream)
+
+    def call_stage1(k, base=0):
+        fs.fs_sample(inp["H"], inp["W"], temperature=inp["temperature"], seeds=inp["seeds"],
+                     vocab_mask=inp["vocab_mask"], offset=base + k, out_tile_max=tmax,
+                     out_tile_idx=tidx, stream=stream, reduce=False)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        import torch.distributed as dist
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    for k in range(max(args.warmup, 3)):
+        call(k)
+    barrier()
+    t_wall0 = time.time()
+    ms = time_calls(lambda k: call(k, args.warmup), args.steps, stream)
+    t_wall1 = time.time()
+    barrier()
+    ms = max_over_ranks(ms)
+    us_call = ms * 1000.0 / args.steps
+
+    # the dominant kernel alone (stage 1), same launches, for the roofline
+    for k in range(3):
+        call_stage1(k)
+    barrier()
+    ms1 = max_over_ranks(time_calls(lambda k: call_stage1(k, args.warmup), args.steps, stream))
+    us_stage1 = ms1 * 1000.0 / args.steps
+    barrier()
+
+    # end to end through the public API: pinned host inputs in, result out
+    Hh = inp["H"].cpu().pin_memory()
+    Th = inp["temperature"].cpu().pin_memory()
+    Sh = inp["seeds"].cpu().pin_memory() if inp["seeds"] is not None else None
+    out_h = torch.empty(B, dtype=torch.int64).pin_memory()
+    Hd = torch.empty_like(inp["H"])
+    Td = torch.empty_like(inp["temperature"])
+    Sd = torch.empty_like(inp["seeds"]) if Sh is not None else None
+
+    def e2e_step(k):
+        Hd.copy_(Hh, non_blocking=True)
+        Td.copy_(Th, non_blocking=True)
+        if Sd is not None:
+            Sd.copy_(Sh, non_blocking=True)
+        fs.fs_sample(Hd, inp["W"], temperature=Td, seeds=Sd, vocab_mask=inp["vocab_mask"],
+                     offset=k, out_idx=out, workspace=ws, stream=stream)
+        out_h.copy_(out, non_blocking=True)
+        stream.synchronize()  # the sampled ids feed the next decode step
+
+    for k in range(3):
+        e2e_step(k)
+    barrier()
+    e2e_steps = max(10, min(args.steps, 500))
+    ms_e2e = max_over_ranks(time_calls(e2e_step, e2e_steps, stream))
+    us_e2e = ms_e2e * 1000.0 / e2e_steps
+    h2d = Hh.numel() * Hh.element_size() + Th.numel() * 4 + (Sh.numel() * 8 if Sh is not None else 0)
+    d2h = out_h.numel() * 8
+
+    # batch sweep of the same head (same run, same W)
+    sweep = []
+    if not args.no_sweep and world == 1:
+        for b2 in w.batches:
+            _, inp2 = make_inputs_like(w, b2, dev, inp["W"])
+            o2 = torch.empty(b2, dtype=torch.int64, device=dev)
+            ws2 = torch.empty(fs.fs_workspace_size(b2, V), dtype=torch.uint8, device=dev)
+            tm2 = torch.empty((b2, nt), dtype=torch.float32, device=dev)
+            ti2 = torch.empty((b2, nt), dtype=torch.int32, device=dev)
+
+            def c2(k):
+                fs.fs_sample(inp2["H"], inp2["W"], temperature=inp2["temperature"],
+                             seeds=inp2["seeds"], offset=k, out_idx=o2, workspace=ws2,
+                             stream=stream)
+
+            def c2s(k):
+                fs.fs_sample(inp2["H"], inp2["W"], temperature=inp2["temperature"],
+                             seeds=inp2["seeds"], offset=k, out_tile_max=tm2, out_tile_idx=ti2,
+                             stream=stream, reduce=False)
+
+            for k in range(5):
+                c2(k)
+            torch.cuda.synchronize()
+            us2 = time_calls(c2, args.sweep_steps, stream) * 1000.0 / args.sweep_steps
+            for k in range(3):
+                c2s(k)
+            us2s = time_calls(c2s, args.sweep_steps, stream) * 1000.0 / args.sweep_steps
+            rf = roofline(b2, d, V, us2s, peaks, seeds=inp2["seeds"] is not None)
+            sweep.append({"B": b2, "us_per_call": round(us2, 2), "us_stage1": round(us2s, 2),
+                          "tokens_per_s": round(b2 / (us2 * 1e-6), 1), "bound": rf["bound"],
+                          "achieved": rf["achieved"], "unit": rf["unit"], "frac": rf["frac"]})
+            del inp2, o2, ws2, tm2, ti2
+    clock_rows = clocks.stop()
+    st, code = fs.fs_last_device_error()
+    if st != fs.FS_OK:
+        raise SystemExit(f"device error word {code} after the benchmark")
+
+    rf = roofline(B, d, V, us_stage1, peaks, traffic=measured_traffic(args.workload, B),
+                  seeds=inp["seeds"] is not None, mask=inp["vocab_mask"] is not None)
+    rf["kernel"] = "fs::stage1_kernel"
+    rf["duration_us"] = round(us_stage1, 3)
+
+    line = {
+        "metric": METRIC,
+        "value": round(us_call, 3),
+        "unit": "us/call",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(us_call / 1000.0, 6),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": f"{w.name} head: d={d} V={V} B={B}, bf16 H~N(0,1) W~N(0,(2/sqrt d)^2), "
+                        "per-row T~U[0.5,1.5] with 10% greedy, per-row seeds, offset=step",
+            "B": B, "d": d, "V": V, "global_batch": B * world,
+            "l2": "inputs exceed L2 (W is %.2f GB), no flush" % (V * d * 2 / 1e9),
+            "parallelism": "replicas" if world > 1 else "single-gpu",
+        },
+        "tokens_per_s": round(B * world / (us_call * 1e-6), 1),
+        "roofline": rf,
+        "e2e": {"value": round(us_e2e, 3), "unit": "us/call",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": 2 * args.steps,
+        "clocks": ClockSampler.summarize(clock_rows, t_wall0, t_wall1),
+        "sweep": sweep,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(inp, B, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def make_inputs_like(w, B, device, W):
+    from lm_head_gumbel_gb300 import workloads as wl
+    H = wl.make_hidden(B, w.d, seed=2000 + B, device=device)
+    T = wl.make_temperature(w, B, seed=3000 + B, device=device)
+    seeds = wl.make_seeds(B, base=4000 + B, device=device) if w.per_row_seeds else None
+    return w, {"H": H, "W": W, "temperature": T, "seeds": seeds, "vocab_mask": None}
+
+
+def oracle_inputs(inp):
+    from lm_head_gumbel_gb300 import workloads as wl
+    return (wl.bf16_bits(inp["H"]), wl.bf16_bits(inp["W"]), inp["temperature"].cpu().numpy(),
+            None if inp["seeds"] is None else wl.u64_bits(inp["seeds"]),
+            None if inp["vocab_mask"] is None else wl.u32_bits(inp["vocab_mask"]))
+
+
+def cpu_baseline(inp, B, budget_s):
+    """The oracle, as it stands, on a bounded sample of the same call: whole
+    rows of the batch until the budget is spent; scaled to one call."""
+    import oracle
+    o = oracle.default()
+    Hb, Wb, T, S, M = oracle_inputs(inp)
+    t0 = time.perf_counter()
+    o.sample(Hb, Wb, temperature=T, seeds=S, mask=M, rows=[0])
+    first = time.perf_counter() - t0
+    n = int(max(1, min(B - 1, budget_s / max(first, 1e-6))))
+    rows = list(range(1, 1 + n))
+    t0 = time.perf_counter()
+    o.sample(Hb, Wb, temperature=T, seeds=S, mask=M, rows=rows)
+    per_row = (time.perf_counter() - t0) / n if n else first
+    return {"value": round(per_row * B * 1e6, 1), "unit": "us/call", "cores": o.num_threads(),
+            "kind": "oracle",
+            "sample": f"{n} of the call's {B} rows (fp64, full vocabulary each), scaled to {B} rows"}
+
+
+def run_reference(args):
+    """The CPU oracle as the reference arm: each step is a bounded sample of
+    the same call (one row, or a vocabulary slice of one row when a row is too
+    slow for the step budget), scaled to the whole call."""
+    world, rank, _ = dist_init("gloo")
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+    import torch
+    import oracle
+    from lm_head_gumbel_gb300 import workloads as wl
+    w = wl.WORKLOADS[args.workload]
+    B, d, V = args.batch, w.d, w.V
+    _, inp = make_inputs(args.workload, B, "cpu")
+    Hb, Wb, T, S, M = oracle_inputs(inp)
+    o = oracle.default()
+    t0 = time.perf_counter()
+    o.sample(Hb, Wb, temperature=T, seeds=S, mask=M, rows=[0])
+    row_s = time.perf_counter() - t0
+    total = args.steps + args.warmup
+    budget = 150.0 / max(total, 1)
+    v_used = V if row_s <= budget else max(128, int(V * budget / row_s) // 128 * 128)
+    Wsub = Wb[:v_used]
+    scale = B * (V / v_used)
+
+    def step(k):
+        r = k % B
+        o.sample(Hb, Wsub, temperature=T, seeds=S, rows=[r], offset=k,
+                 mask=None if M is None else M[:, :(v_used + 31) // 32])
+
+    for k in range(args.warmup):
+        step(k)
+    times = []
+    for k in range(args.steps):
+        t0 = time.perf_counter()
+        step(args.warmup + k)
+        times.append(time.perf_counter() - t0)
+    us = statistics.mean(times) * scale * 1e6
+    sample = (f"1 row of {B} per step" + ("" if v_used == V else f", vocabulary ids 0..{v_used - 1} of {V}")
+              + f"; scaled x{scale:.1f} to one call")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": "us/call",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(statistics.mean(times) * 1000.0, 3), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{w.name} head: d={d} V={V} B={B} (CPU oracle)", "B": B, "d": d,
+                   "V": V, "global_batch": B, "parallelism": "cpu"},
+        "cpu_baseline": {"value": round(us, 1), "unit": "us/call", "cores": o.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(us, 1), "unit": "us/call", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

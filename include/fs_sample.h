@@ -1,0 +1,142 @@
+/*
+ * fs_sample.h -- C ABI of the fused LM-head + exact Gumbel-max sampler
+ * (FlashSampling) for NVIDIA GB300 (sm_103a).
+ *
+ * What one call computes, per batch row b (tomesphere.com, "FlashSampling:
+ * Fast and Memory-Efficient Exact Sampling", Abstract; aitrends.kr write-up,
+ * "Stage 1 (Fused Kernel)" and "Stage 2 (Reduction)"):
+ *
+ *   l[b,v]  = sum_k H[b,k] W[v,k]             LM-head logits, fp32 accumulate
+ *   l'[b,v] = l[b,v] / T_b                    temperature scaling
+ *   s[b,v]  = l'[b,v] + g[b,v]                Gumbel noise g = -log(-log u)
+ *             (-inf where the vocabulary mask clears v)
+ *   tile t = 128 consecutive vocabulary ids:  m_t = max s, i_t = argmax s,
+ *             L_t = log sum exp(l') over the tile's unmasked ids (optional)
+ *   out_idx[b] = argmax_t m_t's index         the sampled token
+ *
+ * The [B,V] logits never reach device memory: they live in the tensor-memory
+ * accumulator of the stage-1 kernel and only (m_t, i_t[, L_t]) leave the chip.
+ * By the Gumbel-max identity the result is an exact sample of
+ * softmax(l'[b,:]) restricted to the unmasked ids (aitrends.kr write-up,
+ * Gumbel-Max paragraph; exactness over tiles because the argmax decomposes
+ * over partitions).
+ *
+ * Conventions fixed by this library where the pages are silent:
+ *   - uniforms: Philox4x32-10 (Salmon et al., SC'11), key = (seed_b low word,
+ *     seed_b high word), counter = (v >> 2, b, offset low word, offset high
+ *     word), output word v & 3; u = ((word >> 9) + 0.5) * 2^-23 in (0,1);
+ *   - T_b <= 0, NaN or +inf selects greedy decoding for row b: s = l, no noise;
+ *   - ties go to the lowest vocabulary index, inside a tile and across tiles;
+ *   - a fully masked tile reports m = -inf, i = -1, L = -inf; a fully masked
+ *     row samples -1;
+ *   - for a greedy row, L_t is the tile's largest unmasked logit.
+ *
+ * Memory: every pointer in fs_sample_args is a DEVICE pointer owned by the
+ * caller; the library allocates no device memory per call.  Calls are
+ * asynchronous on the given stream and never synchronise it.
+ */
+#ifndef FS_SAMPLE_H_
+#define FS_SAMPLE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Vocabulary ids per output tile (the per-tile outputs are [B, ceil(V/128)]). */
+#define FS_TILE 128
+
+typedef enum fs_status {
+  FS_OK = 0,
+  FS_ERR_INVALID_ARG = 1,    /* rejected on the host; nothing was launched   */
+  FS_ERR_UNSUPPORTED = 2,    /* device is not sm_103 (GB300), or no device    */
+  FS_ERR_CUDA = 3,           /* a CUDA runtime/driver call or launch failed   */
+  FS_ERR_DEVICE_TIMEOUT = 4, /* a bounded device-side wait ran out           */
+  FS_ERR_WORKSPACE = 5       /* workspace missing, too small or misaligned    */
+} fs_status;
+
+typedef struct fs_sample_args {
+  /* bf16 [B, d] hidden states, row stride ldh elements.  16-byte aligned base,
+   * ldh % 8 == 0, ldh >= d. */
+  const void *H;
+  /* bf16 [V, d] LM-head weight (nn.Linear layout: one row per token), row
+   * stride ldw elements.  16-byte aligned base, ldw % 8 == 0, ldw >= d. */
+  const void *W;
+  /* fp32 [B] per-row temperature, or NULL for T = 1 on every row. */
+  const float *temperature;
+  /* uint32 [B, mask_ld] packed allow-bits (bit v % 32 of word v / 32 set =
+   * token v may be sampled), or NULL for no mask.  mask_ld >= ceil(V/32). */
+  const uint32_t *vocab_mask;
+  int64_t mask_ld;
+  /* uint64 [B] per-row Philox seeds, or NULL to use `seed` on every row. */
+  const uint64_t *seeds;
+  uint64_t seed;
+  /* Philox counter high words; a decoder advances it once per step. */
+  uint64_t offset;
+  int64_t B, d, V, ldh, ldw;
+  /* int64 [B]: sampled token id per row (-1: row fully masked).  May be NULL
+   * when out_tile_max/out_tile_idx are given: the call then runs stage 1 only
+   * and leaves the per-tile summaries for the caller to merge (e.g. across
+   * vocabulary partitions, the aitrends.kr write-up's tensor-parallel and
+   * Group-Gumbel-Max paragraphs). */
+  int64_t *out_idx;
+  /* Optional per-tile outputs, each [B, ceil(V/128)] row-major, or NULL.
+   * out_tile_max and out_tile_idx are either both given or both NULL. */
+  float *out_tile_max;
+  int32_t *out_tile_idx;
+  float *out_tile_lse; /* given => the kernel also computes L_t */
+  /* Device scratch of at least fs_workspace_size(B, V) bytes, 256-byte
+   * aligned; needed only when out_tile_max/out_tile_idx are NULL. */
+  void *workspace;
+  size_t workspace_bytes;
+} fs_sample_args;
+
+/* Number of 128-wide vocabulary tiles, ceil(V / 128); 0 for V <= 0. */
+int64_t fs_num_tiles(int64_t V);
+
+/* Bytes of workspace fs_sample needs when the caller does not take the
+ * per-tile (max, index) outputs: B * ceil(V/128) * 8, rounded up to 256.
+ * Returns 0 for non-positive sizes. */
+size_t fs_workspace_size(int64_t B, int64_t V);
+
+/*
+ * Sample one token per row (stage 1 + stage 2 above) on `stream` (a
+ * cudaStream_t; NULL = the legacy default stream).  Arguments are checked on
+ * the host first: on FS_ERR_INVALID_ARG / FS_ERR_WORKSPACE / FS_ERR_UNSUPPORTED
+ * nothing is launched and no output is written.  FS_ERR_CUDA reports a failed
+ * launch.  Limits: 1 <= B <= 65535, 1 <= d, 1 <= V < 2^31.
+ * Deterministic: identical inputs, seeds and offset give identical outputs on
+ * every call, stream and graph replay.
+ */
+fs_status fs_sample(const fs_sample_args *args, void *stream);
+
+/*
+ * Diagnostic: the Gumbel noise g[b, v] the stage-1 kernel adds, for rows
+ * [b0, b0+nb) x ids [v0, v0+nv), written to out (device fp32 [nb, nv]).
+ * seeds (device uint64 [b0+nb]) or NULL for `seed` on every row.  Same
+ * Philox/uniform/log chain and the same device code as fs_sample
+ * (aitrends.kr write-up, "Stage 1": g = -log(-log u)).
+ */
+fs_status fs_gumbel_noise(const uint64_t *seeds, uint64_t seed, uint64_t offset,
+                          int64_t b0, int64_t nb, int64_t v0, int64_t nv,
+                          float *out, void *stream);
+
+/*
+ * Read and clear the device-side error word of the current device (this
+ * synchronises the device).  *code receives the raw word (0 = none; bit 0: a
+ * bounded pipeline wait timed out).  Returns FS_ERR_DEVICE_TIMEOUT if a wait
+ * timed out since the last read, FS_OK otherwise, FS_ERR_CUDA on a failed
+ * read.
+ */
+fs_status fs_last_device_error(int *code);
+
+/* Human-readable name of a status code (static storage). */
+const char *fs_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FS_SAMPLE_H_ */

@@ -1,0 +1,182 @@
+"""ctypes binding of ``libfs.so`` (declared in ``include/fs_sample.h``).
+
+Argument marshalling only: tensors become device pointers, sizes and strides;
+every step of the sampling path runs in the library's CUDA kernels.  PyTorch
+provides device memory and the current stream.  When the library has not been
+built, every call raises ``FsError`` -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+FS_TILE = 128
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libfs.so")
+
+FS_OK = 0
+FS_ERR_INVALID_ARG = 1
+FS_ERR_UNSUPPORTED = 2
+FS_ERR_CUDA = 3
+FS_ERR_DEVICE_TIMEOUT = 4
+FS_ERR_WORKSPACE = 5
+
+_c_i64 = ctypes.c_int64
+_c_u64 = ctypes.c_uint64
+_c_ptr = ctypes.c_void_p
+
+
+class FsError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        name = fs_status_string(status) if _lib is not None else str(status)
+        super().__init__(f"{what}: {name}" if what else name)
+
+
+class FsSampleArgs(ctypes.Structure):
+    """Mirror of ``fs_sample_args`` (every field is 8 bytes wide)."""
+    _fields_ = [
+        ("H", _c_ptr), ("W", _c_ptr), ("temperature", _c_ptr),
+        ("vocab_mask", _c_ptr), ("mask_ld", _c_i64), ("seeds", _c_ptr),
+        ("seed", _c_u64), ("offset", _c_u64),
+        ("B", _c_i64), ("d", _c_i64), ("V", _c_i64), ("ldh", _c_i64), ("ldw", _c_i64),
+        ("out_idx", _c_ptr), ("out_tile_max", _c_ptr), ("out_tile_idx", _c_ptr),
+        ("out_tile_lse", _c_ptr), ("workspace", _c_ptr), ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libfs.so (once).  Raises FsError if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise FsError(FS_ERR_UNSUPPORTED,
+                      f"{path} is missing; build it with lm_head_gumbel_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    lib.fs_num_tiles.argtypes = [_c_i64]
+    lib.fs_num_tiles.restype = _c_i64
+    lib.fs_workspace_size.argtypes = [_c_i64, _c_i64]
+    lib.fs_workspace_size.restype = ctypes.c_size_t
+    lib.fs_sample.argtypes = [ctypes.POINTER(FsSampleArgs), _c_ptr]
+    lib.fs_sample.restype = ctypes.c_int
+    lib.fs_gumbel_noise.argtypes = [_c_ptr, _c_u64, _c_u64, _c_i64, _c_i64, _c_i64, _c_i64,
+                                    _c_ptr, _c_ptr]
+    lib.fs_gumbel_noise.restype = ctypes.c_int
+    lib.fs_last_device_error.argtypes = [ctypes.POINTER(ctypes.c_int)]
+    lib.fs_last_device_error.restype = ctypes.c_int
+    lib.fs_status_string.argtypes = [ctypes.c_int]
+    lib.fs_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def fs_num_tiles(V: int) -> int:
+    return int(load_library().fs_num_tiles(int(V)))
+
+
+def fs_workspace_size(B: int, V: int) -> int:
+    return int(load_library().fs_workspace_size(int(B), int(V)))
+
+
+def fs_status_string(status: int) -> str:
+    return load_library().fs_status_string(int(status)).decode()
+
+
+def fs_last_device_error():
+    """(status, raw error word) of the current device; synchronises it."""
+    code = ctypes.c_int(0)
+    st = load_library().fs_last_device_error(ctypes.byref(code))
+    return int(st), int(code.value)
+
+
+def _check_2d(name, t, dtype):
+    if t.dtype != dtype or t.dim() != 2 or t.stride(1) != 1 or not t.is_cuda:
+        raise FsError(FS_ERR_INVALID_ARG, f"{name} must be a CUDA {dtype} matrix with unit column stride")
+
+
+def fs_sample(H, W, *, temperature=None, vocab_mask=None, seeds=None, seed=0, offset=0,
+              out_idx=None, out_tile_max=None, out_tile_idx=None, out_tile_lse=None,
+              workspace=None, stream=None, reduce=True):
+    """Sample one token id per row of H from softmax(H W^T / T) (masked).
+
+    H: bf16 [B, d]; W: bf16 [V, d]; temperature: fp32 [B] or None (T = 1);
+    vocab_mask: int32 [B, >= ceil(V/32)] allow-bits or None; seeds: int64 [B]
+    holding uint64 bit patterns, or None (``seed`` for every row).  Optional
+    per-tile outputs are [B, ceil(V/128)] (fp32 / int32 / fp32).  Returns
+    ``out_idx`` (int64 [B]).  Asynchronous on ``stream`` (default: the
+    current stream of H's device).  With ``reduce=False`` only stage 1 runs:
+    the per-tile outputs (required then) are written and None is returned."""
+    lib = load_library()
+    _check_2d("H", H, torch.bfloat16)
+    _check_2d("W", W, torch.bfloat16)
+    B, d = H.shape
+    V = W.shape[0]
+    dev = H.device
+    if not reduce:
+        if out_tile_max is None or out_tile_idx is None:
+            raise FsError(FS_ERR_INVALID_ARG, "reduce=False needs out_tile_max and out_tile_idx")
+        out_idx = None
+    elif out_idx is None:
+        out_idx = torch.empty(B, dtype=torch.int64, device=dev)
+    mask_ld = 0
+    if vocab_mask is not None:
+        if vocab_mask.dtype != torch.int32 or vocab_mask.dim() != 2 or vocab_mask.stride(1) != 1:
+            raise FsError(FS_ERR_INVALID_ARG, "vocab_mask must be an int32 matrix")
+        mask_ld = vocab_mask.stride(0)
+    if seeds is not None and seeds.dtype != torch.int64:
+        raise FsError(FS_ERR_INVALID_ARG, "seeds must be int64 (uint64 bit patterns)")
+    if temperature is not None and temperature.dtype != torch.float32:
+        raise FsError(FS_ERR_INVALID_ARG, "temperature must be float32")
+    ws_bytes = 0
+    if out_tile_max is None:
+        ws_bytes = fs_workspace_size(B, V)
+        if workspace is None:
+            workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    args = FsSampleArgs(
+        H=_ptr(H), W=_ptr(W), temperature=_ptr(temperature), vocab_mask=_ptr(vocab_mask),
+        mask_ld=mask_ld, seeds=_ptr(seeds), seed=int(seed) & (2**64 - 1),
+        offset=int(offset) & (2**64 - 1), B=B, d=d, V=V, ldh=H.stride(0), ldw=W.stride(0),
+        out_idx=_ptr(out_idx), out_tile_max=_ptr(out_tile_max), out_tile_idx=_ptr(out_tile_idx),
+        out_tile_lse=_ptr(out_tile_lse),
+        workspace=_ptr(workspace) if out_tile_max is None else None,
+        workspace_bytes=(workspace.numel() * workspace.element_size()) if (
+            out_tile_max is None and workspace is not None) else 0)
+    with torch.cuda.device(dev):
+        st = lib.fs_sample(ctypes.byref(args), _stream_handle(stream, dev))
+    if st != FS_OK:
+        raise FsError(st, "fs_sample")
+    return out_idx
+
+
+def fs_gumbel_noise(b0, nb, v0, nv, *, seed=0, offset=0, seeds=None, out=None, device=None,
+                    stream=None):
+    """The fp32 Gumbel noise g[b, v] that fs_sample adds, for a window of
+    rows x vocabulary ids (diagnostic)."""
+    lib = load_library()
+    device = torch.device(device or (seeds.device if seeds is not None else "cuda"))
+    if out is None:
+        out = torch.empty((nb, nv), dtype=torch.float32, device=device)
+    with torch.cuda.device(device):
+        st = lib.fs_gumbel_noise(_ptr(seeds), int(seed) & (2**64 - 1), int(offset) & (2**64 - 1),
+                                 int(b0), int(nb), int(v0), int(nv), _ptr(out),
+                                 _stream_handle(stream, device))
+    if st != FS_OK:
+        raise FsError(st, "fs_gumbel_noise")
+    return out

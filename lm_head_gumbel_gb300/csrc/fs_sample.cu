@@ -1,0 +1,607 @@
+// fs_sample.cu -- fused LM-head + exact Gumbel-max sampling on GB300 (sm_103a).
+//
+// Stage 1 (the aitrends.kr write-up on FlashSampling, "Stage 1 (Fused
+// Kernel)"; tomesphere abstract, "compute logits tile-by-tile on chip, add
+// Gumbel noise, keep only one maximizer per row and per vocabulary tile"):
+// a persistent, warp-specialised kernel.  Each work unit is a 128-row batch
+// block x 256-id vocabulary block of the logits l = H W^T:
+//   warp 0    TMA producer: streams 64-wide K slices of H (128 x 64) and
+//             W (256 x 64) into a 4-stage shared-memory ring (128-byte swizzle)
+//   warp 1    tcgen05 MMA issuer: M=128, N=256, K=16 bf16 MMAs accumulate the
+//             unit's logits in tensor memory (fp32, 256 columns); two
+//             accumulators so the epilogue of one unit overlaps the MMAs of
+//             the next
+//   warps 2-9 epilogue: each thread owns one batch row and 128 vocabulary
+//             columns (one output tile); it reads its logits from tensor
+//             memory, scales by 1/T, masks, adds Philox Gumbel noise, and
+//             keeps the running (max, argmax) and optionally the log-sum-exp
+// Only (m_t, i_t[, L_t]) per (row, 128-id tile) is written to device memory.
+//
+// Stage 2 ("Stage 2 (Reduction)"): one warp per row reduces its tiles to the
+// sampled id, lowest id on ties.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "fs_noise.cuh"
+#include "fs_ptx.cuh"
+#include "fs_sample.h"
+
+namespace fs {
+
+constexpr int kBlockM = 128;   // batch rows per unit = tensor-memory lanes
+constexpr int kBlockN = 256;   // vocabulary ids per unit = accumulator columns
+constexpr int kBlockK = 64;    // bf16 elements per 128-byte swizzled row
+constexpr int kUmmaK = 16;     // K of one kind::f16 MMA
+constexpr int kStages = 4;
+constexpr int kTileV = FS_TILE;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr uint32_t kSmemA = kBlockM * kBlockK * 2;  // H slice, 16 KB
+constexpr uint32_t kSmemB = kBlockN * kBlockK * 2;  // W slice, 32 KB
+constexpr uint32_t kStageBytes = kSmemA + kSmemB;
+constexpr uint32_t kTmemCols = 2 * kBlockN;         // two fp32 accumulators
+constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kBlockM, kBlockN);
+constexpr size_t kBarOffset = size_t(kStages) * kStageBytes;
+constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kBarOffset + 256;
+static_assert(kBlockN == 2 * kTileV, "one unit covers two output tiles");
+static_assert(kBlockK * 2 == 128, "one K slice row is one 128-byte swizzle row");
+
+enum : int { kErrWaitTimeout = 1 };
+
+__device__ int g_error_word = 0;
+
+struct Stage1Params {
+  int32_t B, V, d;
+  int32_t n_tiles;   // ceil(V / 128)
+  int32_t n_mt;      // ceil(B / 128)
+  int32_t n_units;   // ceil(V / 256) * n_mt
+  int32_t n_kb;      // ceil(d / 64)
+  const float* temperature;
+  const uint32_t* mask;
+  int64_t mask_ld;
+  const uint64_t* seeds;
+  uint64_t seed, offset;
+  float* tile_max;
+  int32_t* tile_idx;
+  float* tile_lse;
+  uint64_t wait_limit_ns;
+};
+
+// Bounded mbarrier waits: past the limit the CTA raises its abort flag and
+// the device error word, and every role winds down instead of spinning.
+struct Waiter {
+  volatile uint32_t* abort_flag;
+  uint64_t limit_ns;
+
+  __device__ bool wait(uint64_t* bar, uint32_t parity) const {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::global_timer_ns();
+    while (true) {
+      if (ptx::mbar_try_wait(bar, parity)) return true;
+      if (*abort_flag) return false;
+      if (ptx::global_timer_ns() - t0 > limit_ns) {
+        *abort_flag = 1u;
+        atomicOr(&g_error_word, kErrWaitTimeout);
+        return false;
+      }
+    }
+  }
+  // Used while winding down: ignores the abort flag, still bounded.
+  __device__ bool drain(uint64_t* bar, uint32_t parity) const {
+    const uint64_t t0 = ptx::global_timer_ns();
+    while (!ptx::mbar_try_wait(bar, parity)) {
+      if (ptx::global_timer_ns() - t0 > limit_ns) {
+        atomicOr(&g_error_word, kErrWaitTimeout);
+        return false;
+      }
+    }
+    return true;
+  }
+};
+
+// One thread, one batch row, one 128-id output tile: read the logits from
+// tensor memory 32 columns at a time and reduce them to (m_t, i_t, L_t).
+template <bool kWantLse>
+__device__ __forceinline__ void epilogue_tile(const Stage1Params& p, uint32_t taddr, int row,
+                                              int tile) {
+  const bool valid_row = row < p.B;
+  float T = 1.0f;
+  uint64_t seed = p.seed;
+  const uint32_t* mrow = nullptr;
+  if (valid_row) {
+    if (p.temperature) T = p.temperature[row];
+    if (p.seeds) seed = p.seeds[row];
+    if (p.mask) mrow = p.mask + int64_t(row) * p.mask_ld;
+  }
+  const bool greedy = !(T > 0.0f) || isinf(T);
+  const float inv_t = greedy ? 1.0f : 1.0f / T;
+  const PhiloxKey key{static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32)};
+  const uint32_t ctr_row = static_cast<uint32_t>(row);
+  const uint32_t ctr_off_lo = static_cast<uint32_t>(p.offset);
+  const uint32_t ctr_off_hi = static_cast<uint32_t>(p.offset >> 32);
+
+  float best = -INFINITY;
+  int32_t best_idx = -1;
+  float run_max = -INFINITY, run_sum = 0.0f;  // log-sum-exp state
+  const int v_tile = tile * kTileV;
+
+#pragma unroll 1
+  for (int c = 0; c < kTileV / 32; ++c) {
+    uint32_t r[32];
+    ptx::tmem_ld_32x32b_x32(taddr + uint32_t(c * 32), r);
+    ptx::tmem_wait_ld();
+    if (!valid_row) continue;
+    const int v0 = v_tile + c * 32;
+    uint32_t allow = mrow ? mrow[v0 >> 5] : 0xFFFFFFFFu;
+    const int n_in = p.V - v0;
+    if (n_in < 32) allow &= (n_in <= 0) ? 0u : ((1u << n_in) - 1u);
+
+    float chunk_max = -INFINITY;
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      uint4 rnd = make_uint4(0u, 0u, 0u, 0u);
+      if (!greedy)
+        rnd = philox4x32_10(
+            make_uint4(static_cast<uint32_t>(v0 >> 2) + g, ctr_row, ctr_off_lo, ctr_off_hi), key);
+      const uint32_t words[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int j = g * 4 + i;
+        const float lp = __uint_as_float(r[j]) * inv_t;
+        const float s = greedy ? lp : lp + gumbel_from_word(words[i]);
+        const bool on = (allow >> j) & 1u;
+        if (on && s > best) {
+          best = s;
+          best_idx = v0 + j;
+        }
+        if (kWantLse && on) chunk_max = fmaxf(chunk_max, lp);
+      }
+    }
+    if (kWantLse && chunk_max > -INFINITY) {
+      const float m_new = fmaxf(run_max, chunk_max);
+      float acc = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if ((allow >> j) & 1u) acc += expf(__uint_as_float(r[j]) * inv_t - m_new);
+      run_sum = run_sum * expf(run_max - m_new) + acc;
+      run_max = m_new;
+    }
+  }
+  if (!valid_row) return;
+  const int64_t o = int64_t(row) * p.n_tiles + tile;
+  p.tile_max[o] = best;
+  p.tile_idx[o] = best_idx;
+  if (kWantLse) {
+    float L = run_max;
+    if (!greedy && run_max > -INFINITY) L = run_max + logf(run_sum);
+    p.tile_lse[o] = L;
+  }
+}
+
+template <bool kWantLse>
+__global__ void __launch_bounds__(kThreads, 1)
+    stage1_kernel(const __grid_constant__ CUtensorMap tmap_h,
+                  const __grid_constant__ CUtensorMap tmap_w, const Stage1Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kBarOffset);
+  uint64_t* empty_bar = full_bar + kStages;
+  uint64_t* tfull_bar = empty_bar + kStages;
+  uint64_t* tempty_bar = tfull_bar + 2;
+  uint64_t* drain_bar = tempty_bar + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  volatile uint32_t* abort_flag = tmem_holder + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(&full_bar[s], 1);
+      ptx::mbar_init(&empty_bar[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&tfull_bar[a], 1);
+      ptx::mbar_init(&tempty_bar[a], kEpiWarps);
+    }
+    ptx::mbar_init(drain_bar, 1);
+    *abort_flag = 0u;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tmap_h);
+    ptx::prefetch_tmap(&tmap_w);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_holder, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const Waiter waiter{abort_flag, p.wait_limit_ns};
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      const uint64_t pol_w = p.n_mt > 1 ? ptx::policy_evict_normal() : ptx::policy_evict_first();
+      const uint64_t pol_h = ptx::policy_evict_last();
+      uint32_t stage = 0, phase = 0, issued = 0;
+      bool ok = true;
+      for (int unit = blockIdx.x; ok && unit < p.n_units; unit += gridDim.x) {
+        const int vt = unit / p.n_mt, mt = unit % p.n_mt;
+        for (int kb = 0; kb < p.n_kb; ++kb) {
+          if (!waiter.wait(&empty_bar[stage], phase ^ 1u)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + size_t(stage) * kStageBytes;
+          ptx::mbar_arrive_expect_tx(&full_bar[stage], kStageBytes);
+          ptx::tma_load_2d(sa, &tmap_h, &full_bar[stage], kb * kBlockK, mt * kBlockM, pol_h);
+          ptx::tma_load_2d(sa + kSmemA, &tmap_w, &full_bar[stage], kb * kBlockK, vt * kBlockN,
+                           pol_w);
+          ++issued;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Every issued copy must land before the CTA (and its shared memory)
+      // goes away: wait for the last fill of each stage.
+      for (uint32_t s = 0; s < uint32_t(kStages); ++s) {
+        const uint32_t fills = issued / kStages + (s < issued % kStages ? 1u : 0u);
+        if (fills) waiter.drain(&full_bar[s], (fills - 1u) & 1u);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int unit = blockIdx.x; ok && unit < p.n_units; unit += gridDim.x) {
+        if (!waiter.wait(&tempty_bar[acc], acc_phase ^ 1u)) break;
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * kBlockN;
+        for (int kb = 0; kb < p.n_kb; ++kb) {
+          if (!waiter.wait(&full_bar[stage], phase)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t sa = ptx::smem_u32(smem + size_t(stage) * kStageBytes);
+          const uint32_t sb = sa + kSmemA;
+#pragma unroll
+          for (int k = 0; k < kBlockK / kUmmaK; ++k) {
+            ptx::mma_bf16(d_tmem, ptx::smem_desc_sw128(sa + k * kUmmaK * 2),
+                          ptx::smem_desc_sw128(sb + k * kUmmaK * 2), kIdesc,
+                          (kb | k) != 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(&empty_bar[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit(&tfull_bar[acc]);
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      // All MMAs must be complete before tensor memory is released.
+      ptx::mma_commit(drain_bar);
+      waiter.drain(drain_bar, 0);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue ----------------
+    const int e = warp - 2;
+    const int quad = warp & 3;  // the tensor-memory lane quadrant this warp may read
+    const int half = e >> 2;    // which 128-column half of the unit
+    uint32_t acc = 0, acc_phase = 0;
+    for (int unit = blockIdx.x; unit < p.n_units; unit += gridDim.x) {
+      const int vt = unit / p.n_mt, mt = unit % p.n_mt;
+      int ok = 0;
+      if (lane == 0) ok = waiter.wait(&tfull_bar[acc], acc_phase) ? 1 : 0;
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const int row0 = mt * kBlockM + quad * 32;
+      const int tile = vt * 2 + half;
+      if (row0 < p.B && tile < p.n_tiles) {
+        const uint32_t taddr =
+            tmem_base + (uint32_t(quad * 32) << 16) + acc * kBlockN + uint32_t(half * kTileV);
+        epilogue_tile<kWantLse>(p, taddr, row0 + lane, tile);
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&tempty_bar[acc]);
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// Stage 2: out_idx[b] = i_t* with t* = argmax_t m_t, lowest id on ties.
+__global__ void __launch_bounds__(256) stage2_kernel(const float* __restrict__ tile_max,
+                                                     const int32_t* __restrict__ tile_idx,
+                                                     int32_t B, int32_t n_tiles,
+                                                     int64_t* __restrict__ out_idx) {
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= B) return;
+  const float* m = tile_max + int64_t(row) * n_tiles;
+  const int32_t* ix = tile_idx + int64_t(row) * n_tiles;
+  float best = -INFINITY;
+  int32_t bi = -1;
+  for (int t = lane; t < n_tiles; t += 32) {
+    const int32_t i = ix[t];
+    const float v = m[t];
+    if (i >= 0 && (bi < 0 || v > best)) {
+      best = v;
+      bi = i;
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float ov = __shfl_xor_sync(0xFFFFFFFFu, best, off);
+    const int32_t oi = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
+    if (oi >= 0 && (bi < 0 || ov > best || (ov == best && oi < bi))) {
+      best = ov;
+      bi = oi;
+    }
+  }
+  if (lane == 0) out_idx[row] = bi;
+}
+
+// The noise stage 1 adds, element by element (diagnostic entry point).
+__global__ void noise_kernel(const uint64_t* __restrict__ seeds, uint64_t seed, uint64_t offset,
+                             int64_t b0, int64_t nb, int64_t v0, int64_t nv,
+                             float* __restrict__ out) {
+  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= nb * nv) return;
+  const int64_t b = b0 + i / nv, v = v0 + i % nv;
+  const uint64_t sd = seeds ? seeds[b] : seed;
+  const uint4 r = philox4x32_10(
+      make_uint4(static_cast<uint32_t>(v >> 2), static_cast<uint32_t>(b),
+                 static_cast<uint32_t>(offset), static_cast<uint32_t>(offset >> 32)),
+      PhiloxKey{static_cast<uint32_t>(sd), static_cast<uint32_t>(sd >> 32)});
+  out[i] = gumbel_from_word(select_word(r, static_cast<uint32_t>(v & 3)));
+}
+
+// ----------------------------------------------------------------------------
+// Host side
+// ----------------------------------------------------------------------------
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+constexpr int kMaxDevices = 64;
+struct DeviceState {
+  bool initialised = false;
+  fs_status status = FS_ERR_UNSUPPORTED;
+  int num_sms = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_devices[kMaxDevices];
+EncodeTiledFn g_encode = nullptr;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+fs_status device_setup(int* num_sms) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return FS_ERR_UNSUPPORTED;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& st = g_devices[dev];
+  if (!st.initialised) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return FS_ERR_CUDA;
+    }
+    st.num_sms = sms;
+    if (major != 10 || minor != 3) {
+      st.status = FS_ERR_UNSUPPORTED;
+    } else {
+      st.status = FS_OK;
+      if (cudaFuncSetAttribute(stage1_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               int(kSmemBytes)) != cudaSuccess ||
+          cudaFuncSetAttribute(stage1_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               int(kSmemBytes)) != cudaSuccess) {
+        cudaGetLastError();
+        st.status = FS_ERR_CUDA;
+      }
+      if (st.status == FS_OK && g_encode == nullptr) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr) {
+          cudaGetLastError();
+          st.status = FS_ERR_CUDA;
+        } else {
+          g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+        }
+      }
+    }
+    st.initialised = true;
+  }
+  *num_sms = st.num_sms;
+  return st.status;
+}
+
+// 2-D bf16 tensor map: inner extent `inner` (contiguous), `outer` rows of
+// `row_bytes`; boxes of box_inner x box_outer with the 128-byte swizzle;
+// out-of-range elements read as zero.
+bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+}  // namespace fs
+
+using namespace fs;
+
+extern "C" int64_t fs_num_tiles(int64_t V) { return V <= 0 ? 0 : (V + kTileV - 1) / kTileV; }
+
+extern "C" size_t fs_workspace_size(int64_t B, int64_t V) {
+  if (B <= 0 || V <= 0) return 0;
+  const size_t bytes = size_t(B) * size_t(fs_num_tiles(V)) * 8u;
+  return (bytes + 255u) & ~size_t(255u);
+}
+
+extern "C" const char* fs_status_string(int status) {
+  switch (status) {
+    case FS_OK: return "FS_OK";
+    case FS_ERR_INVALID_ARG: return "FS_ERR_INVALID_ARG";
+    case FS_ERR_UNSUPPORTED: return "FS_ERR_UNSUPPORTED";
+    case FS_ERR_CUDA: return "FS_ERR_CUDA";
+    case FS_ERR_DEVICE_TIMEOUT: return "FS_ERR_DEVICE_TIMEOUT";
+    case FS_ERR_WORKSPACE: return "FS_ERR_WORKSPACE";
+    default: return "FS_ERR_UNKNOWN";
+  }
+}
+
+extern "C" fs_status fs_sample(const fs_sample_args* a, void* stream_ptr) {
+  if (a == nullptr) return FS_ERR_INVALID_ARG;
+  const int64_t B = a->B, d = a->d, V = a->V;
+  if (!a->H || !a->W) return FS_ERR_INVALID_ARG;
+  if (!a->out_idx && !a->out_tile_max) return FS_ERR_INVALID_ARG;
+  if (B < 1 || B > 65535 || d < 1 || V < 1 || V > int64_t(0x7FFFFFFF)) return FS_ERR_INVALID_ARG;
+  if (d > int64_t(0x7FFFFFFF) - kBlockK) return FS_ERR_INVALID_ARG;
+  if (a->ldh < d || a->ldw < d || a->ldh % 8 != 0 || a->ldw % 8 != 0) return FS_ERR_INVALID_ARG;
+  if (!aligned(a->H, 16) || !aligned(a->W, 16)) return FS_ERR_INVALID_ARG;
+  if (a->out_idx && !aligned(a->out_idx, 8)) return FS_ERR_INVALID_ARG;
+  if (a->temperature && !aligned(a->temperature, 4)) return FS_ERR_INVALID_ARG;
+  if (a->seeds && !aligned(a->seeds, 8)) return FS_ERR_INVALID_ARG;
+  if (a->vocab_mask && (!aligned(a->vocab_mask, 4) || a->mask_ld < (V + 31) / 32))
+    return FS_ERR_INVALID_ARG;
+  if ((a->out_tile_max == nullptr) != (a->out_tile_idx == nullptr)) return FS_ERR_INVALID_ARG;
+  if (a->out_tile_max && (!aligned(a->out_tile_max, 4) || !aligned(a->out_tile_idx, 4)))
+    return FS_ERR_INVALID_ARG;
+  if (a->out_tile_lse && !aligned(a->out_tile_lse, 4)) return FS_ERR_INVALID_ARG;
+
+  const int64_t n_tiles = fs_num_tiles(V);
+  float* tmax = a->out_tile_max;
+  int32_t* tidx = a->out_tile_idx;
+  if (tmax == nullptr) {
+    const size_t need = fs_workspace_size(B, V);
+    if (!a->workspace || a->workspace_bytes < need || !aligned(a->workspace, 256))
+      return FS_ERR_WORKSPACE;
+    tmax = static_cast<float*>(a->workspace);
+    tidx = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(a->workspace) +
+                                      size_t(B) * size_t(n_tiles) * 4u);
+  }
+
+  int num_sms = 0;
+  const fs_status st = device_setup(&num_sms);
+  if (st != FS_OK) return st;
+
+  CUtensorMap tmap_h, tmap_w;
+  if (!encode_2d(&tmap_h, a->H, uint64_t(d), uint64_t(B), uint64_t(a->ldh) * 2u, kBlockK,
+                 kBlockM) ||
+      !encode_2d(&tmap_w, a->W, uint64_t(d), uint64_t(V), uint64_t(a->ldw) * 2u, kBlockK,
+                 kBlockN))
+    return FS_ERR_INVALID_ARG;
+
+  Stage1Params p;
+  p.B = int32_t(B);
+  p.V = int32_t(V);
+  p.d = int32_t(d);
+  p.n_tiles = int32_t(n_tiles);
+  p.n_mt = int32_t((B + kBlockM - 1) / kBlockM);
+  p.n_units = int32_t((V + kBlockN - 1) / kBlockN) * p.n_mt;
+  p.n_kb = int32_t((d + kBlockK - 1) / kBlockK);
+  p.temperature = a->temperature;
+  p.mask = a->vocab_mask;
+  p.mask_ld = a->mask_ld;
+  p.seeds = a->seeds;
+  p.seed = a->seed;
+  p.offset = a->offset;
+  p.tile_max = tmax;
+  p.tile_idx = tidx;
+  p.tile_lse = a->out_tile_lse;
+  p.wait_limit_ns = kWaitLimitNs;
+
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  const int grid = p.n_units < num_sms ? p.n_units : num_sms;
+  if (a->out_tile_lse)
+    stage1_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(tmap_h, tmap_w, p);
+  else
+    stage1_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(tmap_h, tmap_w, p);
+  if (cudaGetLastError() != cudaSuccess) return FS_ERR_CUDA;
+
+  if (a->out_idx == nullptr) return FS_OK;  // stage 1 only
+  const int rows_per_block = 256 / 32;
+  stage2_kernel<<<int((B + rows_per_block - 1) / rows_per_block), 256, 0, stream>>>(
+      tmax, tidx, int32_t(B), int32_t(n_tiles), a->out_idx);
+  if (cudaGetLastError() != cudaSuccess) return FS_ERR_CUDA;
+  return FS_OK;
+}
+
+extern "C" fs_status fs_gumbel_noise(const uint64_t* seeds, uint64_t seed, uint64_t offset,
+                                     int64_t b0, int64_t nb, int64_t v0, int64_t nv, float* out,
+                                     void* stream_ptr) {
+  if (!out || b0 < 0 || nb < 0 || v0 < 0 || nv < 0) return FS_ERR_INVALID_ARG;
+  if (b0 + nb > int64_t(0xFFFFFFFF) || v0 + nv > int64_t(0x7FFFFFFF)) return FS_ERR_INVALID_ARG;
+  if (nb == 0 || nv == 0) return FS_OK;
+  int num_sms = 0;
+  const fs_status st = device_setup(&num_sms);
+  if (st != FS_OK) return st;
+  const int64_t n = nb * nv;
+  const int threads = 256;
+  const int64_t blocks = (n + threads - 1) / threads;
+  if (blocks > int64_t(0x7FFFFFFF)) return FS_ERR_INVALID_ARG;
+  noise_kernel<<<unsigned(blocks), threads, 0, static_cast<cudaStream_t>(stream_ptr)>>>(
+      seeds, seed, offset, b0, nb, v0, nv, out);
+  return cudaGetLastError() == cudaSuccess ? FS_OK : FS_ERR_CUDA;
+}
+
+extern "C" fs_status fs_last_device_error(int* code) {
+  int v = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpyFromSymbol(&v, g_error_word, sizeof(int)) != cudaSuccess) {
+    cudaGetLastError();
+    return FS_ERR_CUDA;
+  }
+  const int zero = 0;
+  if (v != 0 && cudaMemcpyToSymbol(g_error_word, &zero, sizeof(int)) != cudaSuccess) {
+    cudaGetLastError();
+    return FS_ERR_CUDA;
+  }
+  if (code) *code = v;
+  return (v & kErrWaitTimeout) ? FS_ERR_DEVICE_TIMEOUT : FS_OK;
+}

@@ -1,0 +1,118 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/fs_sample.h declares, and rejects bad arguments on the host before
+any device work (these calls return before touching CUDA)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fs_sample.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from lm_head_gumbel_gb300 import build as libbuild
+    try:
+        libbuild.build()
+    except RuntimeError as e:  # no nvcc on this machine
+        pytest.skip(str(e))
+    import lm_head_gumbel_gb300 as fs
+    return fs.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fs_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for want in ("fs_sample", "fs_workspace_size", "fs_num_tiles", "fs_status_string",
+                 "fs_gumbel_noise", "fs_last_device_error"):
+        assert want in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_exports_are_c_symbols():
+    """No C++ mangling on the entry points (checked with nm on the .so)."""
+    import shutil
+    import subprocess
+    from lm_head_gumbel_gb300 import LIB_PATH
+    if not shutil.which("nm") or not os.path.exists(LIB_PATH):
+        pytest.skip("nm or library missing")
+    out = subprocess.run(["nm", "-D", "--defined-only", LIB_PATH], capture_output=True,
+                         text=True).stdout
+    syms = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in declared_functions():
+        assert name in syms, name
+
+
+def test_host_helpers(lib):
+    import lm_head_gumbel_gb300 as fs
+    assert fs.fs_num_tiles(1) == 1
+    assert fs.fs_num_tiles(128) == 1
+    assert fs.fs_num_tiles(129) == 2
+    assert fs.fs_num_tiles(151936) == 1187
+    assert fs.fs_num_tiles(0) == 0
+    assert fs.fs_workspace_size(4, 4096) == 1024
+    assert fs.fs_workspace_size(3, 129) == 256
+    assert fs.fs_workspace_size(512, 151936) == ((512 * 1187 * 8 + 255) // 256) * 256
+    assert fs.fs_workspace_size(0, 10) == 0
+    for code, name in ((0, "FS_OK"), (1, "FS_ERR_INVALID_ARG"), (2, "FS_ERR_UNSUPPORTED"),
+                       (3, "FS_ERR_CUDA"), (4, "FS_ERR_DEVICE_TIMEOUT"), (5, "FS_ERR_WORKSPACE")):
+        assert fs.fs_status_string(code) == name
+    assert fs.fs_status_string(99) == "FS_ERR_UNKNOWN"
+
+
+def _args(**kw):
+    import lm_head_gumbel_gb300 as fs
+    base = dict(H=0x10000, W=0x20000, out_idx=0x30000, B=4, d=256, V=4096, ldh=256, ldw=256,
+                out_tile_max=0x40000, out_tile_idx=0x50000)
+    base.update(kw)
+    return fs.FsSampleArgs(**base)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(H=None), 1), (dict(W=None), 1), (dict(out_idx=None, out_tile_max=None), 1),
+    (dict(B=0), 1), (dict(B=65536), 1), (dict(d=0), 1), (dict(V=0), 1), (dict(V=2**31), 1),
+    (dict(ldh=255), 1), (dict(ldh=260), 1), (dict(ldw=128), 1),
+    (dict(H=0x10002), 1), (dict(W=0x20008), 1), (dict(out_idx=0x30004), 1),
+    (dict(out_tile_idx=None), 1), (dict(out_tile_max=None), 1),
+    (dict(vocab_mask=0x60000, mask_ld=127), 1),
+    (dict(out_tile_max=None, out_tile_idx=None), 5),
+    (dict(out_tile_max=None, out_tile_idx=None, workspace=0x70000, workspace_bytes=255), 5),
+    (dict(out_tile_max=None, out_tile_idx=None, workspace=0x70080, workspace_bytes=4096), 5),
+])
+def test_bad_arguments_rejected_on_host(lib, kw, want):
+    a = _args(**kw)
+    assert lib.fs_sample(ctypes.byref(a), None) == want
+
+
+def test_null_args_rejected(lib):
+    assert lib.fs_sample(None, None) == 1
+
+
+def test_noise_bad_arguments(lib):
+    assert lib.fs_gumbel_noise(None, 0, 0, 0, 1, 0, 1, None, None) == 1
+    assert lib.fs_gumbel_noise(None, 0, 0, -1, 1, 0, 1, ctypes.c_void_p(0x1000), None) == 1
+    # an empty window is a no-op
+    assert lib.fs_gumbel_noise(None, 0, 0, 0, 0, 0, 5, ctypes.c_void_p(0x1000), None) == 0
+
+
+def test_package_fails_loudly_without_library(tmp_path):
+    """With the library missing, the binding raises instead of falling back."""
+    import lm_head_gumbel_gb300._binding as bnd
+    saved = bnd._lib
+    bnd._lib = None
+    try:
+        with pytest.raises(bnd.FsError):
+            bnd.load_library(str(tmp_path / "missing.so"))
+    finally:
+        bnd._lib = saved

@@ -1,0 +1,138 @@
+"""The synthetic workloads at full size, in the launch configuration the
+benchmark times: sampled rows against the oracle (which computes them one by
+one), and properties that hold at any size on every row."""
+import numpy as np
+import pytest
+import torch
+
+import lm_head_gumbel_gb300 as fs
+from lm_head_gumbel_gb300 import workloads as wl
+from oracle import merge
+from gpu_cases import assert_no_device_error, compare, make_problem, run_device
+
+pytestmark = pytest.mark.gpu
+
+_W_CACHE = {}
+
+
+def weights(name):
+    """Device W of a workload and its host bit patterns (one copy each)."""
+    if name not in _W_CACHE:
+        _W_CACHE.clear()
+        torch.cuda.empty_cache()
+        w = wl.WORKLOADS[name]
+        W = wl.make_weights(w.d, w.V, seed=77, device="cuda", outlier_frac=w.outlier_frac)
+        _W_CACHE[name] = (W, wl.bf16_bits(W))
+    return _W_CACHE[name]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    fs.load_library()
+    yield
+    _W_CACHE.clear()
+    assert_no_device_error()
+
+
+def sample_rows(B, k=4, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = {0, B - 1} | set(rng.integers(0, B, size=k).tolist())
+    return sorted(rows)
+
+
+def whole_batch_properties(prob, dev, V):
+    idx, tmax, tidx = dev["idx"], dev["tile_max"], dev["tile_idx"]
+    B, nt = tmax.shape
+    assert idx.shape == (B,)
+    assert np.all((idx >= -1) & (idx < V))
+    # stage 2 is the exact argmax over tiles (lowest id on ties)
+    for b in range(B):
+        ok = tidx[b] >= 0
+        if not ok.any():
+            assert idx[b] == -1
+            continue
+        m = np.where(ok, tmax[b], -np.inf)
+        t = int(np.argmax(m))
+        assert idx[b] == tidx[b, t]
+    # every per-tile argmax lies in its tile
+    t_of = np.arange(nt)[None, :]
+    valid = tidx >= 0
+    assert np.all((tidx[valid] // 128) == np.broadcast_to(t_of, tidx.shape)[valid])
+    if prob["vocab_mask"] is not None:
+        m = prob["vocab_mask"].cpu().numpy().view(np.uint32)
+        sel = idx >= 0
+        bits = (m[np.arange(B)[sel], idx[sel] // 32] >> (idx[sel] % 32)) & 1
+        assert np.all(bits == 1), "a masked token was sampled"
+
+
+@pytest.mark.parametrize("B", [1, 8, 32, 128, 256])
+def test_qwen3_1_7b_head(B):
+    W, Wb = weights("qwen3-1.7b")
+    p = make_problem(B, W.shape[1], W.shape[0], T=0.7, seed=B, W=W)
+    for step in (0, 1):
+        dev = run_device(p, seed=2024, offset=step, lse=False)
+        whole_batch_properties(p, dev, W.shape[0])
+        compare(p, dev, sample_rows(B, seed=step), seed=2024, offset=step, W_bits=Wb)
+
+
+@pytest.mark.parametrize("B", [1, 16, 64, 256, 512])
+def test_qwen3_8b_head(B):
+    """Per-row temperatures (10% greedy), per-row seeds, decode steps with the
+    offset advancing: every step runs; sampled steps go to the oracle."""
+    W, Wb = weights("qwen3-8b")
+    p = make_problem(B, W.shape[1], W.shape[0], T="row-uniform", per_row_seeds=True, seed=B, W=W)
+    steps = 1000 if B <= 64 else 50
+    checked = (0, 1, steps // 2, steps - 1)
+    out = torch.empty((steps, B), dtype=torch.int64, device="cuda")
+    ws = torch.empty(fs.fs_workspace_size(B, W.shape[0]), dtype=torch.uint8, device="cuda")
+    for step in range(steps):
+        fs.fs_sample(p["H"], W, temperature=p["temperature"], seeds=p["seeds"], offset=step,
+                     out_idx=out[step], workspace=ws)
+    torch.cuda.synchronize()
+    out = out.cpu().numpy()
+    assert np.all((out >= 0) & (out < W.shape[0]))
+    greedy = (p["temperature"].cpu().numpy() <= 0)
+    if greedy.any():  # greedy rows do not depend on the step
+        assert np.all(out[:, greedy] == out[0:1, greedy])
+    for step in checked:
+        dev = run_device(p, seed=0, offset=step, lse=False)
+        assert np.array_equal(dev["idx"], out[step])
+        whole_batch_properties(p, dev, W.shape[0])
+        compare(p, dev, sample_rows(B, k=2, seed=step), offset=step, seed=0, W_bits=Wb)
+
+
+def test_llama3_8b_masked_head():
+    W, Wb = weights("llama3-8b-mask")
+    B = 128
+    p = make_problem(B, W.shape[1], W.shape[0], T=1.0, mask_frac=0.05, seed=3, W=W)
+    dev = run_device(p, seed=31, offset=9, lse=True)
+    whole_batch_properties(p, dev, W.shape[0])
+    compare(p, dev, sample_rows(B), seed=31, offset=9, W_bits=Wb)
+
+
+@pytest.mark.parametrize("B", [512, 1024])
+def test_large_vocab_head_partition_merge(B):
+    """d=5120, V=262144: the tile log-sum-exps merged over 4 equal vocabulary
+    partitions reproduce the row log-mass, and the exact merge over the
+    partitions' maxima reproduces the sampled id on every row."""
+    W, Wb = weights("large-vocab")
+    V = W.shape[0]
+    p = make_problem(B, W.shape[1], V, T=0.8, seed=B, W=W)
+    dev = run_device(p, seed=55, offset=1, lse=True)
+    whole_batch_properties(p, dev, V)
+    nt = dev["tile_max"].shape[1]
+    bounds = [0, nt // 4, nt // 2, 3 * nt // 4, nt]
+    for b in range(B):
+        i, _ = merge.partition_argmax(dev["tile_max"][b], dev["tile_idx"][b], bounds)
+        assert i == dev["idx"][b]
+    st = compare(p, dev, sample_rows(B, k=2), seed=55, offset=1, W_bits=Wb)
+    assert st["max_abs_tile_lse"] < 2e-3
+    rows = sample_rows(B, k=2)
+    from gpu_cases import run_oracle
+    ref = run_oracle(p, rows, seed=55, offset=1, W_bits=Wb)
+    for r, b in enumerate(rows):
+        parts = [merge.lse_merge(dev["tile_lse"][b, bounds[k]:bounds[k + 1]]) for k in range(4)]
+        whole = merge.lse_merge(ref["tile_lse"][r])
+        assert abs(merge.lse_merge(parts) - whole) < 2e-3

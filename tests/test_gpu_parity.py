@@ -1,0 +1,185 @@
+"""CUDA path (through the C ABI) against the CPU oracle on small and ragged
+problems, element by element: sampled ids, per-tile maxima, argmaxes and
+log-sum-exps (gate and tolerances in oracle/parity.py)."""
+import math
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import lm_head_gumbel_gb300 as fs
+from lm_head_gumbel_gb300 import workloads as wl
+import oracle
+from oracle import merge, parity
+from gpu_cases import assert_no_device_error, compare, make_problem, run_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    fs.load_library()
+    yield
+    assert_no_device_error()
+
+
+def test_noise_matches_oracle():
+    """Device Philox + Gumbel vs the oracle's fp64 chain on a window that spans
+    several Philox blocks, rows, per-row seeds and a high offset word."""
+    o = oracle.default()
+    for (seed, offset, seeds) in ((0, 0, None), (123456789123, (7 << 32) + 3, None),
+                                  (0, 99, np.array([5, 2**63 + 11, 0, 2**40], np.uint64))):
+        sd_t = None if seeds is None else torch.from_numpy(seeds.view(np.int64)).cuda()
+        g = fs.fs_gumbel_noise(0, 4, 1000, 777, seed=seed, offset=offset, seeds=sd_t)
+        torch.cuda.synchronize()
+        want = o.noise_grid(0, 4, 1000, 777, seed=seed, offset=offset, seeds=seeds)
+        err = np.abs(g.cpu().numpy().astype(np.float64) - want)
+        assert err.max() < 2e-5, err.max()
+
+
+def test_noise_accuracy_over_all_uniforms():
+    """The fp32 noise is within 1e-5 of the fp64 value for every one of the
+    2^23 uniform levels (vocabulary ids cover all words of many blocks)."""
+    o = oracle.default()
+    g = fs.fs_gumbel_noise(0, 1, 0, 1 << 21, seed=42, offset=1).cpu().numpy().ravel()
+    sub = np.arange(0, 1 << 21, 997)
+    want = np.array([o.noise(42, 1, 0, int(v)) for v in sub])
+    assert np.abs(g[sub] - want).max() < 2e-5
+    assert np.all(np.isfinite(g)) and g.min() > -3.0 and g.max() < 17.0
+
+
+@pytest.mark.parametrize("T", [1.0, 0.0, 0.7])
+def test_tiny(T):
+    """B=4, d=256, V=4096: every row and tile, noisy and greedy."""
+    p = make_problem(4, 256, 4096, T=T, seed=1)
+    dev = run_device(p, seed=0, offset=0)
+    st = compare(p, dev, seed=0, offset=0, scores=True)
+    assert st["rows_gated"] >= 3
+
+
+@pytest.mark.parametrize("B,d,V", [
+    (1, 8, 1), (1, 8, 2), (3, 72, 100), (1, 264, 1000), (5, 64, 129), (2, 136, 4097),
+    (7, 200, 255), (33, 96, 257), (129, 64, 640), (130, 128, 3000), (300, 64, 1100),
+])
+def test_ragged_shapes(B, d, V):
+    """Odd B (several 128-row blocks), d not a multiple of 64, V with a
+    ragged last tile and a ragged last 256-id unit."""
+    p = make_problem(B, d, V, T=0.9, seed=B + d + V)
+    dev = run_device(p, seed=3, offset=5)
+    compare(p, dev, seed=3, offset=5, scores=True)
+
+
+def test_mixed_rows_seeds_mask():
+    """Per-row seeds, per-row temperatures with greedy rows, a vocab mask with
+    fully masked tiles and a fully masked row."""
+    B, d, V = 40, 128, 2000
+    p = make_problem(B, d, V, T="row-uniform", per_row_seeds=True, mask_frac=0.05, seed=9)
+    m = p["vocab_mask"]
+    m[3, :] = 0                      # row 3: nothing allowed
+    m[5, 4:8] = 0                    # row 5: tile 1 fully masked
+    dev = run_device(p, offset=17)
+    assert dev["idx"][3] == -1
+    assert np.all(dev["tile_idx"][5, 1] == -1)
+    compare(p, dev, offset=17, scores=True)
+
+
+def test_outliers_and_lse():
+    """W rows scaled by 4 (heavy logits) with the tile log-sum-exp output."""
+    p = make_problem(16, 256, 3000, T=1.0, outlier_frac=0.03, mask_frac=0.05, seed=4)
+    dev = run_device(p, offset=2)
+    st = compare(p, dev, offset=2, scores=True)
+    assert st["max_abs_tile_lse"] < parity.TOL_LSE
+
+
+def test_workspace_path_matches_tile_outputs():
+    p = make_problem(20, 64, 5000, T=0.8, seed=5)
+    a = run_device(p, offset=3, lse=False, tiles=False)
+    b = run_device(p, offset=3, lse=True, tiles=True)
+    assert np.array_equal(a["idx"], b["idx"])
+
+
+def test_deterministic_across_calls_and_streams():
+    p = make_problem(64, 128, 6000, T=1.0, seed=6)
+    a = run_device(p, offset=11)
+    s = torch.cuda.Stream()
+    b = run_device(p, offset=11, stream=s)
+    c = run_device(p, offset=11)
+    for k in a:
+        assert np.array_equal(a[k], b[k]) and np.array_equal(a[k], c[k]), k
+    d = run_device(p, offset=12)
+    assert not np.array_equal(a["idx"], d["idx"])
+
+
+def test_graph_replay_matches_eager():
+    p = make_problem(8, 64, 3000, T=1.0, seed=8)
+    eager = run_device(p, offset=4)["idx"]
+    out = torch.empty(8, dtype=torch.int64, device="cuda")
+    ws = torch.empty(fs.fs_workspace_size(8, 3000), dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        fs.fs_sample(p["H"], p["W"], temperature=p["temperature"], seed=7, offset=4,
+                     out_idx=out, workspace=ws)  # first call sets the device up
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        fs.fs_sample(p["H"], p["W"], temperature=p["temperature"], seed=7, offset=4,
+                     out_idx=out, workspace=ws)
+    for _ in range(3):
+        out.fill_(-5)
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(out.cpu().numpy(), eager)
+
+
+def test_chi_square_on_device():
+    """Device draws over many offsets follow softmax(l/T) (Pearson
+    chi-square), and equal the oracle's draws offset by offset."""
+    V, d, T, n = 16, 64, 0.8, 6000
+    p = make_problem(1, d, V, T=T, seed=12)
+    out = torch.empty(1, dtype=torch.int64, device="cuda")
+    ws = torch.empty(fs.fs_workspace_size(1, V), dtype=torch.uint8, device="cuda")
+    draws = torch.empty(n, dtype=torch.int64, device="cuda")
+    for off in range(n):
+        fs.fs_sample(p["H"], p["W"], temperature=p["temperature"], seed=99, offset=off,
+                     out_idx=draws[off:off + 1], workspace=ws)
+    torch.cuda.synchronize()
+    draws = draws.cpu().numpy()
+    o = oracle.default()
+    Hb, Wb = wl.bf16_bits(p["H"]), wl.bf16_bits(p["W"])
+    logits = o.logits(Hb, Wb)[0]
+    probs = scipy.special.softmax(logits / float(np.float32(T)))
+    _, _, pval = merge.chi_square_gof(np.bincount(draws, minlength=V), probs)
+    assert pval > 1e-3, pval
+    agree = 0
+    for off in range(0, n, 10):
+        r = o.sample(Hb, Wb, temperature=p["temperature"].cpu().numpy(), seed=99, offset=off)
+        if r["gap"][0] > parity.GAP:
+            assert draws[off] == r["idx"][0], off
+            agree += 1
+    assert agree > 0.9 * (n // 10)
+
+
+def test_group_merge_on_device_tiles():
+    """Group-Gumbel-Max over 4 vocabulary partitions, fed the device's per-tile
+    (max, argmax, log-sum-exp), reproduces the distribution, and the exact
+    partition argmax equals the flat sample."""
+    V, d, T, n = 512, 32, 1.0, 2000
+    p = make_problem(1, d, V, T=T, seed=13)
+    probs = None
+    rng = np.random.default_rng(0)
+    hier = []
+    for off in range(n):
+        dev = run_device(p, seed=5, offset=off)
+        tm, ti, tl = dev["tile_max"][0], dev["tile_idx"][0], dev["tile_lse"][0]
+        i, _ = merge.partition_argmax(tm, ti, [0, 1, 2, 3, 4])
+        assert i == dev["idx"][0]
+        hier.append(merge.group_gumbel_max(ti, tl, rng.random(4)))
+        if probs is None:
+            Hb, Wb = wl.bf16_bits(p["H"]), wl.bf16_bits(p["W"])
+            probs = scipy.special.softmax(oracle.default().logits(Hb, Wb)[0] / T)
+    counts = np.bincount(np.asarray(hier), minlength=V)
+    _, _, pval = merge.chi_square_gof(counts, probs)
+    assert pval > 1e-3, pval
