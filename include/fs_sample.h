@@ -112,6 +112,38 @@ size_t fs_workspace_size(int64_t B, int64_t V);
  */
 fs_status fs_sample(const fs_sample_args *args, void *stream);
 
+/* Size of the library's built-in scratch array used by fs_sample_noalloc. */
+#define FS_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20) /* 8 MiB */
+
+/*
+ * fs_sample for callers that cannot allocate device memory.  (The FlashSampling
+ * pages have no counterpart to this entry point; it is a deployment aid.)
+ *
+ * Some callers cannot call cudaMalloc: a sampler plugged into an inference
+ * engine that reserves the whole device for its own memory pool and hands its
+ * plugins no allocator, or a decode loop that cannot afford cudaMalloc's
+ * implicit device synchronisation.  This entry point computes exactly what
+ * fs_sample computes, but instead of args->workspace (ignored, like
+ * args->workspace_bytes) it uses a scratch array of FS_NOALLOC_SCRATCH_BYTES
+ * that lives inside the library: a file-scope __device__ array that every GPU
+ * which loads the library holds until the process exits.  The caller still
+ * owns and passes every input and output.  The library calls no cudaMalloc,
+ * cudaFree or other allocating routine on this path.
+ *
+ * - Limit: when out_tile_max/out_tile_idx are NULL the scratch must hold
+ *   fs_workspace_size(B, V) bytes; larger problems return FS_ERR_WORKSPACE
+ *   before anything is launched.  With per-tile outputs given no scratch is
+ *   used and fs_sample's limits apply.
+ * - Set-up: the first call on a device (with that device current) looks up the
+ *   array's device address once; make that first call before any stream
+ *   capture.
+ * - Sharing: every call on a device uses the same array, which keeps the last
+ *   call's contents (nothing in it needs to start at zero: stage 1 writes
+ *   every entry stage 2 reads).  Calls that overlap on the GPU (concurrent
+ *   streams) race on it; serialise them.
+ */
+fs_status fs_sample_noalloc(const fs_sample_args *args, void *stream);
+
 /*
  * Diagnostic: the Gumbel noise g[b, v] the stage-1 kernel adds, for rows
  * [b0, b0+nb) x ids [v0, v0+nv), written to out (device fp32 [nb, nv]).

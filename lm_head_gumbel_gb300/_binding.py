@@ -64,6 +64,8 @@ def load_library(path: str = LIB_PATH):
     lib.fs_workspace_size.restype = ctypes.c_size_t
     lib.fs_sample.argtypes = [ctypes.POINTER(FsSampleArgs), _c_ptr]
     lib.fs_sample.restype = ctypes.c_int
+    lib.fs_sample_noalloc.argtypes = [ctypes.POINTER(FsSampleArgs), _c_ptr]
+    lib.fs_sample_noalloc.restype = ctypes.c_int
     lib.fs_gumbel_noise.argtypes = [_c_ptr, _c_u64, _c_u64, _c_i64, _c_i64, _c_i64, _c_i64,
                                     _c_ptr, _c_ptr]
     lib.fs_gumbel_noise.restype = ctypes.c_int

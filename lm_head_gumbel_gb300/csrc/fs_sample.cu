@@ -572,6 +572,59 @@ extern "C" fs_status fs_sample(const fs_sample_args* a, void* stream_ptr) {
   return FS_OK;
 }
 
+// ---- allocation-free variant ---------------------------------------------
+// Scratch of fs_sample_noalloc: a file-scope device array, so callers that
+// cannot allocate device memory still have the stage-1 -> stage-2 workspace.
+// In host code `g_noalloc_scratch` is only a host-side stand-in for the symbol;
+// its device address is looked up once per device with cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[FS_NOALLOC_SCRATCH_BYTES];
+
+namespace fs {
+namespace {
+void* g_noalloc_addr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device (looked up on the
+// first call per device).
+fs_status noalloc_scratch(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return FS_ERR_UNSUPPORTED;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_noalloc_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return FS_ERR_CUDA;
+    }
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return FS_OK;
+}
+}  // namespace
+}  // namespace fs
+
+extern "C" fs_status fs_sample_noalloc(const fs_sample_args* a, void* stream_ptr) {
+  if (a == nullptr) return FS_ERR_INVALID_ARG;
+  if (a->out_tile_max == nullptr) {  // the built-in scratch must hold the workspace
+    if (a->B < 1 || a->B > 65535 || a->V < 1 || a->V > int64_t(0x7FFFFFFF))
+      return FS_ERR_INVALID_ARG;
+    if (fs_workspace_size(a->B, a->V) > FS_NOALLOC_SCRATCH_BYTES) return FS_ERR_WORKSPACE;
+  }
+  int num_sms = 0;
+  const fs_status st = device_setup(&num_sms);
+  if (st != FS_OK) return st;
+  void* scratch = nullptr;
+  const fs_status st2 = noalloc_scratch(&scratch);
+  if (st2 != FS_OK) return st2;
+  fs_sample_args b = *a;
+  b.workspace = scratch;
+  b.workspace_bytes = FS_NOALLOC_SCRATCH_BYTES;
+  return fs_sample(&b, stream_ptr);
+}
+
 extern "C" fs_status fs_gumbel_noise(const uint64_t* seeds, uint64_t seed, uint64_t offset,
                                      int64_t b0, int64_t nb, int64_t v0, int64_t nv, float* out,
                                      void* stream_ptr) {
