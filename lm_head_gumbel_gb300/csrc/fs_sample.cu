@@ -5,8 +5,9 @@
 // Gumbel noise, keep only one maximizer per row and per vocabulary tile"):
 // a persistent, warp-specialised kernel.  Each work unit is a 128-row batch
 // block x 256-id vocabulary block of the logits l = H W^T:
-//   warp 0    TMA producer: streams 64-wide K slices of H (128 x 64) and
-//             W (256 x 64) into a 4-stage shared-memory ring (128-byte swizzle)
+//   warp 0    TMA producer: streams 64-wide K slices of W (256 x 64) and
+//             H (up to 128 x 64) into a 4-stage shared-memory ring (128-byte
+//             swizzle)
 //   warp 1    tcgen05 MMA issuer: M=128, N=256, K=16 bf16 MMAs accumulate the
 //             unit's logits in tensor memory (fp32, 256 columns); two
 //             accumulators so the epilogue of one unit overlaps the MMAs of
@@ -70,6 +71,7 @@ struct Stage1Params {
   int32_t* tile_idx;
   float* tile_lse;
   uint64_t wait_limit_ns;
+  uint32_t h_box_rows;  // rows of the H box: min(128, B rounded up to 8)
 };
 
 // Bounded mbarrier waits: past the limit the CTA raises its abort flag and
@@ -104,11 +106,19 @@ struct Waiter {
   }
 };
 
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // One thread, one batch row, one 128-id output tile: read the logits from
-// tensor memory 32 columns at a time and reduce them to (m_t, i_t, L_t).
+// tensor memory 32 columns at a time and reduce them to (m_t, i_t[, L_t]).
+// Scores are s = l * (1/T) + g (one fma); the log-sum-exp is kept in base 2.
 template <bool kWantLse>
 __device__ __forceinline__ void epilogue_tile(const Stage1Params& p, uint32_t taddr, int row,
                                               int tile) {
+  constexpr float kLog2e = 1.4426950408889634f, kLn2 = 0.6931471805599453f;
   const bool valid_row = row < p.B;
   float T = 1.0f;
   uint64_t seed = p.seed;
@@ -120,14 +130,15 @@ __device__ __forceinline__ void epilogue_tile(const Stage1Params& p, uint32_t ta
   }
   const bool greedy = !(T > 0.0f) || isinf(T);
   const float inv_t = greedy ? 1.0f : 1.0f / T;
-  const PhiloxKey key{static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32)};
+  const float inv_t_log2e = inv_t * kLog2e;
+  const PhiloxSchedule ks(seed);
   const uint32_t ctr_row = static_cast<uint32_t>(row);
   const uint32_t ctr_off_lo = static_cast<uint32_t>(p.offset);
   const uint32_t ctr_off_hi = static_cast<uint32_t>(p.offset >> 32);
 
   float best = -INFINITY;
   int32_t best_idx = -1;
-  float run_max = -INFINITY, run_sum = 0.0f;  // log-sum-exp state
+  float run_max = -INFINITY, run_sum = 0.0f;  // base-2 log-sum-exp state
   const int v_tile = tile * kTileV;
 
 #pragma unroll 1
@@ -141,35 +152,47 @@ __device__ __forceinline__ void epilogue_tile(const Stage1Params& p, uint32_t ta
     const int n_in = p.V - v0;
     if (n_in < 32) allow &= (n_in <= 0) ? 0u : ((1u << n_in) - 1u);
 
-    float chunk_max = -INFINITY;
+    if (greedy) {  // s = l, no noise; L_t = max l
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float l = __uint_as_float(r[j]);
+        if (((allow >> j) & 1u) && l > best) {
+          best = l;
+          best_idx = v0 + j;
+        }
+      }
+      continue;
+    }
 #pragma unroll
     for (int g = 0; g < 8; ++g) {
-      uint4 rnd = make_uint4(0u, 0u, 0u, 0u);
-      if (!greedy)
-        rnd = philox4x32_10(
-            make_uint4(static_cast<uint32_t>(v0 >> 2) + g, ctr_row, ctr_off_lo, ctr_off_hi), key);
+      const uint4 rnd = philox4x32_10(
+          make_uint4(static_cast<uint32_t>(v0 >> 2) + g, ctr_row, ctr_off_lo, ctr_off_hi), ks);
       const uint32_t words[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int j = g * 4 + i;
-        const float lp = __uint_as_float(r[j]) * inv_t;
-        const float s = greedy ? lp : lp + gumbel_from_word(words[i]);
-        const bool on = (allow >> j) & 1u;
-        if (on && s > best) {
+        const float s = fmaf(__uint_as_float(r[j]), inv_t, gumbel_from_word(words[i]));
+        if (((allow >> j) & 1u) && s > best) {
           best = s;
           best_idx = v0 + j;
         }
-        if (kWantLse && on) chunk_max = fmaxf(chunk_max, lp);
       }
     }
-    if (kWantLse && chunk_max > -INFINITY) {
-      const float m_new = fmaxf(run_max, chunk_max);
-      float acc = 0.0f;
+    if (kWantLse) {
+      float cm = -INFINITY;
 #pragma unroll
       for (int j = 0; j < 32; ++j)
-        if ((allow >> j) & 1u) acc += expf(__uint_as_float(r[j]) * inv_t - m_new);
-      run_sum = run_sum * expf(run_max - m_new) + acc;
-      run_max = m_new;
+        if ((allow >> j) & 1u) cm = fmaxf(cm, __uint_as_float(r[j]) * inv_t_log2e);
+      if (cm > -INFINITY) {
+        const float m_new = fmaxf(run_max, cm);
+        float acc = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if ((allow >> j) & 1u)
+            acc += ex2_approx(fmaf(__uint_as_float(r[j]), inv_t_log2e, -m_new));
+        run_sum = fmaf(run_sum, ex2_approx(run_max - m_new), acc);
+        run_max = m_new;
+      }
     }
   }
   if (!valid_row) return;
@@ -177,8 +200,8 @@ __device__ __forceinline__ void epilogue_tile(const Stage1Params& p, uint32_t ta
   p.tile_max[o] = best;
   p.tile_idx[o] = best_idx;
   if (kWantLse) {
-    float L = run_max;
-    if (!greedy && run_max > -INFINITY) L = run_max + logf(run_sum);
+    float L = best;  // greedy rows: the largest unmasked logit
+    if (!greedy) L = run_max > -INFINITY ? (run_max + __log2f(run_sum)) * kLn2 : -INFINITY;
     p.tile_lse[o] = L;
   }
 }
@@ -237,16 +260,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int unit = blockIdx.x; ok && unit < p.n_units; unit += gridDim.x) {
         const int vt = unit / p.n_mt, mt = unit % p.n_mt;
-        for (int kb = 0; kb < p.n_kb; ++kb) {
+        // Each vocabulary block starts its K loop at its own slice, so CTAs
+        // working at the same moment read different H lines.  The start
+        // depends on the vocabulary block only, so a row's sums (and its
+        // sample) do not depend on the batch size.
+        const int k_start = int((uint32_t(vt) * 5u) % uint32_t(p.n_kb));
+        for (int kk = 0; kk < p.n_kb; ++kk) {
+          const int kb = kk + k_start < p.n_kb ? kk + k_start : kk + k_start - p.n_kb;
           if (!waiter.wait(&empty_bar[stage], phase ^ 1u)) {
             ok = false;
             break;
           }
           uint8_t* sa = smem + size_t(stage) * kStageBytes;
-          ptx::mbar_arrive_expect_tx(&full_bar[stage], kStageBytes);
-          ptx::tma_load_2d(sa, &tmap_h, &full_bar[stage], kb * kBlockK, mt * kBlockM, pol_h);
+          ptx::mbar_arrive_expect_tx(&full_bar[stage], kSmemB + p.h_box_rows * 128u);
           ptx::tma_load_2d(sa + kSmemA, &tmap_w, &full_bar[stage], kb * kBlockK, vt * kBlockN,
                            pol_w);
+          ptx::tma_load_2d(sa, &tmap_h, &full_bar[stage], kb * kBlockK, mt * kBlockM, pol_h);
           ++issued;
           if (++stage == kStages) {
             stage = 0;
@@ -380,7 +409,7 @@ __global__ void noise_kernel(const uint64_t* __restrict__ seeds, uint64_t seed, 
   const uint4 r = philox4x32_10(
       make_uint4(static_cast<uint32_t>(v >> 2), static_cast<uint32_t>(b),
                  static_cast<uint32_t>(offset), static_cast<uint32_t>(offset >> 32)),
-      PhiloxKey{static_cast<uint32_t>(sd), static_cast<uint32_t>(sd >> 32)});
+      PhiloxSchedule(sd));
   out[i] = gumbel_from_word(select_word(r, static_cast<uint32_t>(v & 3)));
 }
 
@@ -530,9 +559,13 @@ extern "C" fs_status fs_sample(const fs_sample_args* a, void* stream_ptr) {
   const fs_status st = device_setup(&num_sms);
   if (st != FS_OK) return st;
 
+  // H box: only the rows that exist (rounded up to the 8-row swizzle atom);
+  // the MMA's remaining A rows hold stale data and only feed accumulator rows
+  // that are never read.
+  const uint32_t h_rows = B >= kBlockM ? uint32_t(kBlockM) : uint32_t((B + 7) / 8 * 8);
   CUtensorMap tmap_h, tmap_w;
   if (!encode_2d(&tmap_h, a->H, uint64_t(d), uint64_t(B), uint64_t(a->ldh) * 2u, kBlockK,
-                 kBlockM) ||
+                 h_rows) ||
       !encode_2d(&tmap_w, a->W, uint64_t(d), uint64_t(V), uint64_t(a->ldw) * 2u, kBlockK,
                  kBlockN))
     return FS_ERR_INVALID_ARG;
@@ -555,6 +588,7 @@ extern "C" fs_status fs_sample(const fs_sample_args* a, void* stream_ptr) {
   p.tile_idx = tidx;
   p.tile_lse = a->out_tile_lse;
   p.wait_limit_ns = kWaitLimitNs;
+  p.h_box_rows = h_rows;
 
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   const int grid = p.n_units < num_sms ? p.n_units : num_sms;
