@@ -60,7 +60,8 @@ struct Stage1Params {
   int32_t B, V, d;
   int32_t n_tiles;   // ceil(V / 128)
   int32_t n_mt;      // ceil(B / 128)
-  int32_t n_units;   // ceil(V / 256) * n_mt
+  int32_t n_mgroups; // ceil(n_mt / cluster size)
+  int32_t n_cunits;  // ceil(V / 256) * n_mgroups: units of work per cluster
   int32_t n_kb;      // ceil(d / 64)
   const float* temperature;
   const uint32_t* mask;
@@ -206,10 +207,20 @@ __device__ __forceinline__ void epilogue_tile(const Stage1Params& p, uint32_t ta
   }
 }
 
-template <bool kWantLse>
+// Work decomposition: a unit is (vocabulary block vt of 256 ids, batch block mt
+// of 128 rows).  CTAs run in clusters of kCluster along the batch dimension: the
+// CTAs of a cluster take the kCluster batch blocks of one group of one
+// vocabulary block, each loads 1/kCluster of the W slice and multicasts it to
+// the whole cluster, so W crosses L2 -> SM once per cluster instead of once per
+// CTA.  A stage is refilled only after every CTA of the cluster has consumed it
+// (the MMA commits are multicast to every CTA's "empty" barrier).
+template <bool kWantLse, int kCluster>
 __global__ void __launch_bounds__(kThreads, 1)
     stage1_kernel(const __grid_constant__ CUtensorMap tmap_h,
                   const __grid_constant__ CUtensorMap tmap_w, const Stage1Params p) {
+  static_assert(kCluster == 1 || kCluster == 2 || kCluster == 4, "cluster of 1, 2 or 4 CTAs");
+  constexpr uint32_t kRowsW = kBlockN / kCluster;  // W rows this CTA loads per stage
+  constexpr uint16_t kMask = uint16_t((1u << kCluster) - 1u);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -223,11 +234,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int rank = kCluster > 1 ? int(ptx::cluster_ctarank()) : 0;
+  const int cluster_id = int(blockIdx.x) / kCluster;
+  const int n_clusters = int(gridDim.x) / kCluster;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&full_bar[s], 1);
-      ptx::mbar_init(&empty_bar[s], 1);
+      ptx::mbar_init(&empty_bar[s], kCluster);
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&tfull_bar[a], 1);
@@ -248,18 +262,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
+  // Every CTA's barriers exist before any peer multicasts into them.
+  if (kCluster > 1) ptx::cluster_sync();
   const uint32_t tmem_base = *tmem_holder;
   const Waiter waiter{abort_flag, p.wait_limit_ns};
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      const uint64_t pol_w = p.n_mt > 1 ? ptx::policy_evict_normal() : ptx::policy_evict_first();
+      const uint64_t pol_w = p.n_mt > kCluster ? ptx::policy_evict_normal()
+                                               : ptx::policy_evict_first();
       const uint64_t pol_h = ptx::policy_evict_last();
       uint32_t stage = 0, phase = 0, issued = 0;
       bool ok = true;
-      for (int unit = blockIdx.x; ok && unit < p.n_units; unit += gridDim.x) {
-        const int vt = unit / p.n_mt, mt = unit % p.n_mt;
+      for (int cu = cluster_id; ok && cu < p.n_cunits; cu += n_clusters) {
+        const int vt = cu / p.n_mgroups;
+        const int mt = (cu % p.n_mgroups) * kCluster + rank;
         // Each vocabulary block starts its K loop at its own slice, so CTAs
         // working at the same moment read different H lines.  The start
         // depends on the vocabulary block only, so a row's sums (and its
@@ -273,8 +291,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t* sa = smem + size_t(stage) * kStageBytes;
           ptx::mbar_arrive_expect_tx(&full_bar[stage], kSmemB + p.h_box_rows * 128u);
-          ptx::tma_load_2d(sa + kSmemA, &tmap_w, &full_bar[stage], kb * kBlockK, vt * kBlockN,
-                           pol_w);
+          if (kCluster == 1) {
+            ptx::tma_load_2d(sa + kSmemA, &tmap_w, &full_bar[stage], kb * kBlockK, vt * kBlockN,
+                             pol_w);
+          } else {
+            // In the last vocabulary block a slice may start past V; it is
+            // then read from the last valid row instead (those ids are masked
+            // in the epilogue), so no box lies wholly outside the tensor.
+            const int wy = min(vt * kBlockN + rank * int(kRowsW), p.V - 1);
+            ptx::tma_load_2d_multicast(sa + kSmemA + rank * kRowsW * 128u, &tmap_w,
+                                       &full_bar[stage], kb * kBlockK, wy, kMask, pol_w);
+          }
           ptx::tma_load_2d(sa, &tmap_h, &full_bar[stage], kb * kBlockK, mt * kBlockM, pol_h);
           ++issued;
           if (++stage == kStages) {
@@ -296,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
-      for (int unit = blockIdx.x; ok && unit < p.n_units; unit += gridDim.x) {
+      for (int cu = cluster_id; ok && cu < p.n_cunits; cu += n_clusters) {
         if (!waiter.wait(&tempty_bar[acc], acc_phase ^ 1u)) break;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * kBlockN;
@@ -314,7 +341,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                           ptx::smem_desc_sw128(sb + k * kUmmaK * 2), kIdesc,
                           (kb | k) != 0 ? 1u : 0u);
           }
-          ptx::mma_commit(&empty_bar[stage]);
+          if (kCluster == 1)
+            ptx::mma_commit(&empty_bar[stage]);
+          else
+            ptx::mma_commit_multicast(&empty_bar[stage], kMask);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
@@ -336,8 +366,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;  // the tensor-memory lane quadrant this warp may read
     const int half = e >> 2;    // which 128-column half of the unit
     uint32_t acc = 0, acc_phase = 0;
-    for (int unit = blockIdx.x; unit < p.n_units; unit += gridDim.x) {
-      const int vt = unit / p.n_mt, mt = unit % p.n_mt;
+    for (int cu = cluster_id; cu < p.n_cunits; cu += n_clusters) {
+      const int vt = cu / p.n_mgroups;
+      const int mt = (cu % p.n_mgroups) * kCluster + rank;
       int ok = 0;
       if (lane == 0) ok = waiter.wait(&tfull_bar[acc], acc_phase) ? 1 : 0;
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
@@ -364,6 +395,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, kTmemCols);
   }
+  // No CTA leaves while a peer may still multicast into it or arrive on its
+  // barriers.
+  if (kCluster > 1) ptx::cluster_sync();
 }
 
 // Stage 2: out_idx[b] = i_t* with t* = argmax_t m_t, lowest id on ties.
@@ -428,12 +462,69 @@ struct DeviceState {
   bool initialised = false;
   fs_status status = FS_ERR_UNSUPPORTED;
   int num_sms = 0;
+  int max_clusters[2][3] = {};  // [want_lse][log2 cluster size]: co-resident clusters
 };
 
 std::mutex g_mu;
 DeviceState g_devices[kMaxDevices];
 EncodeTiledFn g_encode = nullptr;
+thread_local const DeviceState* g_last_state = nullptr;  // set by device_setup
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+constexpr int log2_cluster(int c) { return c == 1 ? 0 : c == 2 ? 1 : 2; }
+
+cudaLaunchConfig_t launch_config(int cluster, cudaLaunchAttribute* attr, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = unsigned(cluster);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+// Opt one stage-1 variant into its shared memory and record how many of its
+// clusters fit on the device at once (the persistent grid size).
+template <bool kWantLse, int kCluster>
+bool prepare_variant(DeviceState& st, int sms) {
+  auto kern = stage1_kernel<kWantLse, kCluster>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes)) !=
+      cudaSuccess)
+    return false;
+  int n = sms / kCluster;
+  if (kCluster > 1) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) !=
+        cudaSuccess)
+      return false;
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = launch_config(kCluster, attr, nullptr);
+    cfg.gridDim = dim3(unsigned(n * kCluster), 1, 1);
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) return false;
+  }
+  st.max_clusters[kWantLse ? 1 : 0][log2_cluster(kCluster)] = n;
+  return true;
+}
+
+template <bool kWantLse, int kCluster>
+fs_status launch_stage1(const CUtensorMap& tmap_h, const CUtensorMap& tmap_w, Stage1Params p,
+                        int max_clusters, cudaStream_t stream) {
+  p.n_mgroups = (p.n_mt + kCluster - 1) / kCluster;
+  p.n_cunits = int32_t((int64_t(p.V) + kBlockN - 1) / kBlockN) * p.n_mgroups;
+  const int clusters = p.n_cunits < max_clusters ? p.n_cunits : max_clusters;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = launch_config(kCluster, attr, stream);
+  cfg.gridDim = dim3(unsigned(clusters * kCluster), 1, 1);
+  if (cudaLaunchKernelEx(&cfg, stage1_kernel<kWantLse, kCluster>, tmap_h, tmap_w, p) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return FS_ERR_CUDA;
+  }
+  return FS_OK;
+}
 
 fs_status device_setup(int* num_sms) {
   int dev = -1;
@@ -456,10 +547,9 @@ fs_status device_setup(int* num_sms) {
       st.status = FS_ERR_UNSUPPORTED;
     } else {
       st.status = FS_OK;
-      if (cudaFuncSetAttribute(stage1_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               int(kSmemBytes)) != cudaSuccess ||
-          cudaFuncSetAttribute(stage1_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               int(kSmemBytes)) != cudaSuccess) {
+      if (!prepare_variant<false, 1>(st, sms) || !prepare_variant<true, 1>(st, sms) ||
+          !prepare_variant<false, 2>(st, sms) || !prepare_variant<true, 2>(st, sms) ||
+          !prepare_variant<false, 4>(st, sms) || !prepare_variant<true, 4>(st, sms)) {
         cudaGetLastError();
         st.status = FS_ERR_CUDA;
       }
@@ -479,6 +569,7 @@ fs_status device_setup(int* num_sms) {
     st.initialised = true;
   }
   *num_sms = st.num_sms;
+  g_last_state = &st;
   return st.status;
 }
 
@@ -563,11 +654,15 @@ extern "C" fs_status fs_sample(const fs_sample_args* a, void* stream_ptr) {
   // the MMA's remaining A rows hold stale data and only feed accumulator rows
   // that are never read.
   const uint32_t h_rows = B >= kBlockM ? uint32_t(kBlockM) : uint32_t((B + 7) / 8 * 8);
+  const int n_mt = int((B + kBlockM - 1) / kBlockM);
+  // Clusters of 2 CTAs along the batch share (multicast) the W slice; used when
+  // the batch blocks pair up exactly.
+  const int cluster = (n_mt % 2 == 0) ? 2 : 1;
   CUtensorMap tmap_h, tmap_w;
   if (!encode_2d(&tmap_h, a->H, uint64_t(d), uint64_t(B), uint64_t(a->ldh) * 2u, kBlockK,
                  h_rows) ||
       !encode_2d(&tmap_w, a->W, uint64_t(d), uint64_t(V), uint64_t(a->ldw) * 2u, kBlockK,
-                 kBlockN))
+                 uint32_t(kBlockN / cluster)))
     return FS_ERR_INVALID_ARG;
 
   Stage1Params p;
@@ -575,8 +670,9 @@ extern "C" fs_status fs_sample(const fs_sample_args* a, void* stream_ptr) {
   p.V = int32_t(V);
   p.d = int32_t(d);
   p.n_tiles = int32_t(n_tiles);
-  p.n_mt = int32_t((B + kBlockM - 1) / kBlockM);
-  p.n_units = int32_t((V + kBlockN - 1) / kBlockN) * p.n_mt;
+  p.n_mt = int32_t(n_mt);
+  p.n_mgroups = 0;  // set per variant at launch
+  p.n_cunits = 0;
   p.n_kb = int32_t((d + kBlockK - 1) / kBlockK);
   p.temperature = a->temperature;
   p.mask = a->vocab_mask;
@@ -591,12 +687,17 @@ extern "C" fs_status fs_sample(const fs_sample_args* a, void* stream_ptr) {
   p.h_box_rows = h_rows;
 
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
-  const int grid = p.n_units < num_sms ? p.n_units : num_sms;
-  if (a->out_tile_lse)
-    stage1_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(tmap_h, tmap_w, p);
+  const DeviceState& ds = *g_last_state;
+  const bool lse = a->out_tile_lse != nullptr;
+  const int mc = ds.max_clusters[lse ? 1 : 0][log2_cluster(cluster)];
+  fs_status lst;
+  if (cluster == 2)
+    lst = lse ? launch_stage1<true, 2>(tmap_h, tmap_w, p, mc, stream)
+              : launch_stage1<false, 2>(tmap_h, tmap_w, p, mc, stream);
   else
-    stage1_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(tmap_h, tmap_w, p);
-  if (cudaGetLastError() != cudaSuccess) return FS_ERR_CUDA;
+    lst = lse ? launch_stage1<true, 1>(tmap_h, tmap_w, p, mc, stream)
+              : launch_stage1<false, 1>(tmap_h, tmap_w, p, mc, stream);
+  if (lst != FS_OK) return lst;
 
   if (a->out_idx == nullptr) return FS_OK;  // stage 1 only
   const int rows_per_block = 256 / 32;
