@@ -1,7 +1,7 @@
 #!/usr/bin/env python
 """Benchmark of the fused LM-head + exact Gumbel-max sampler (one GPU per rank).
 
-A step is one fs_sample call (stage 1 + stage 2) over one batch of the
+A step is one fs_sample call (one fused kernel launch) over one batch of the
 synthetic Qwen3-8B-shaped head (d=4096, V=151936): per-row temperatures
 U[0.5,1.5] with 10% greedy rows, per-row seeds, the Philox offset advancing by
 one per step.  W (1.24 GB) exceeds L2, so every step streams it from HBM.
@@ -60,15 +60,13 @@ def load_peaks():
     return dict(FALLBACK_PEAKS, source="fallback")
 
 
-def algorithmic(B, d, V, *, mask=False, lse=False, seeds=True, temperature=True):
-    """Bytes and flops one stage-1 launch must move / do: W and H once, the
-    per-row parameters, the mask bits, and the per-tile outputs."""
-    nt = (V + 127) // 128
-    by = V * d * 2 + B * d * 2 + B * nt * 8
+def algorithmic(B, d, V, *, mask=False, seeds=True, temperature=True):
+    """Bytes and flops one sampling call must move / do: W and H once, the
+    per-row parameters and mask bits, and the sampled ids (int64)."""
+    by = V * d * 2 + B * d * 2 + B * 8
     by += B * 4 if temperature else 0
     by += B * 8 if seeds else 0
     by += B * ((V + 31) // 32) * 4 if mask else 0
-    by += B * nt * 4 if lse else 0
     return by, 2.0 * B * V * d
 
 
@@ -228,22 +226,14 @@ def run_ours(args):
     B = args.batch
     w, inp = make_inputs(args.workload, B, dev)
     d, V = w.d, w.V
-    nt = fs.fs_num_tiles(V)
     stream = torch.cuda.current_stream(dev)
     out = torch.empty(B, dtype=torch.int64, device=dev)
-    ws = torch.empty(fs.fs_workspace_size(B, V), dtype=torch.uint8, device=dev)
-    tmax = torch.empty((B, nt), dtype=torch.float32, device=dev)
-    tidx = torch.empty((B, nt), dtype=torch.int32, device=dev)
+    ws = torch.zeros(fs.fs_workspace_size(B, V), dtype=torch.uint8, device=dev)
 
     def call(k, base=0):
         fs.fs_sample(inp["H"], inp["W"], temperature=inp["temperature"], seeds=inp["seeds"],
                      vocab_mask=inp["vocab_mask"], offset=base + k, out_idx=out, workspace=ws,
                      stream=stream)
-
-    def call_stage1(k, base=0):
-        fs.fs_sample(inp["H"], inp["W"], temperature=inp["temperature"], seeds=inp["seeds"],
-                     vocab_mask=inp["vocab_mask"], offset=base + k, out_tile_max=tmax,
-                     out_tile_idx=tidx, stream=stream, reduce=False)
 
     def barrier():
         torch.cuda.synchronize()
@@ -272,13 +262,6 @@ def run_ours(args):
     ms = max_over_ranks(ms)
     us_call = ms * 1000.0 / args.steps
 
-    # the dominant kernel alone (stage 1), same launches, for the roofline
-    for k in range(3):
-        call_stage1(k)
-    barrier()
-    ms1 = max_over_ranks(time_calls(lambda k: call_stage1(k, args.warmup), args.steps, stream))
-    us_stage1 = ms1 * 1000.0 / args.steps
-    barrier()
 
     # end to end through the public API: pinned host inputs in, result out
     Hh = inp["H"].cpu().pin_memory()
@@ -314,41 +297,36 @@ def run_ours(args):
         for b2 in w.batches:
             _, inp2 = make_inputs_like(w, b2, dev, inp["W"])
             o2 = torch.empty(b2, dtype=torch.int64, device=dev)
-            ws2 = torch.empty(fs.fs_workspace_size(b2, V), dtype=torch.uint8, device=dev)
-            tm2 = torch.empty((b2, nt), dtype=torch.float32, device=dev)
-            ti2 = torch.empty((b2, nt), dtype=torch.int32, device=dev)
+            ws2 = torch.zeros(fs.fs_workspace_size(b2, V), dtype=torch.uint8, device=dev)
 
             def c2(k):
                 fs.fs_sample(inp2["H"], inp2["W"], temperature=inp2["temperature"],
                              seeds=inp2["seeds"], offset=k, out_idx=o2, workspace=ws2,
                              stream=stream)
 
-            def c2s(k):
-                fs.fs_sample(inp2["H"], inp2["W"], temperature=inp2["temperature"],
-                             seeds=inp2["seeds"], offset=k, out_tile_max=tm2, out_tile_idx=ti2,
-                             stream=stream, reduce=False)
-
             for k in range(5):
                 c2(k)
             torch.cuda.synchronize()
+            ts0 = time.time()
             us2 = time_calls(c2, args.sweep_steps, stream) * 1000.0 / args.sweep_steps
-            for k in range(3):
-                c2s(k)
-            us2s = time_calls(c2s, args.sweep_steps, stream) * 1000.0 / args.sweep_steps
-            rf = roofline(b2, d, V, us2s, peaks, seeds=inp2["seeds"] is not None)
-            sweep.append({"B": b2, "us_per_call": round(us2, 2), "us_stage1": round(us2s, 2),
+            rf = roofline(b2, d, V, us2, peaks, seeds=inp2["seeds"] is not None)
+            sweep.append({"B": b2, "us_per_call": round(us2, 2),
                           "tokens_per_s": round(b2 / (us2 * 1e-6), 1), "bound": rf["bound"],
-                          "achieved": rf["achieved"], "unit": rf["unit"], "frac": rf["frac"]})
-            del inp2, o2, ws2, tm2, ti2
+                          "achieved": rf["achieved"], "unit": rf["unit"], "frac": rf["frac"],
+                          "window": (ts0, time.time())})
+            del inp2, o2, ws2
     clock_rows = clocks.stop()
+    for ent in sweep:  # clocks seen while each batch size ran
+        c = ClockSampler.summarize(clock_rows, *ent.pop("window"))
+        ent["sm_mhz"] = None if c is None else c["sm_mhz"]
     st, code = fs.fs_last_device_error()
     if st != fs.FS_OK:
         raise SystemExit(f"device error word {code} after the benchmark")
 
-    rf = roofline(B, d, V, us_stage1, peaks, traffic=measured_traffic(args.workload, B),
+    rf = roofline(B, d, V, us_call, peaks, traffic=measured_traffic(args.workload, B),
                   seeds=inp["seeds"] is not None, mask=inp["vocab_mask"] is not None)
-    rf["kernel"] = "fs::stage1_kernel"
-    rf["duration_us"] = round(us_stage1, 3)
+    rf["kernel"] = "fs::stage1_kernel (the whole call: stage 2 is fused into it)"
+    rf["duration_us"] = round(us_call, 3)
 
     line = {
         "metric": METRIC,
@@ -374,7 +352,7 @@ def run_ours(args):
         "roofline": rf,
         "e2e": {"value": round(us_e2e, 3), "unit": "us/call",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": args.steps,
         "clocks": ClockSampler.summarize(clock_rows, t_wall0, t_wall1),
         "sweep": sweep,
     }

@@ -12,10 +12,11 @@
  *             (-inf where the vocabulary mask clears v)
  *   tile t = 128 consecutive vocabulary ids:  m_t = max s, i_t = argmax s,
  *             L_t = log sum exp(l') over the tile's unmasked ids (optional)
- *   out_idx[b] = argmax_t m_t's index         the sampled token
+ *   out_idx[b] = the id of max_t m_t          the sampled token
  *
  * The [B,V] logits never reach device memory: they live in the tensor-memory
- * accumulator of the stage-1 kernel and only (m_t, i_t[, L_t]) leave the chip.
+ * accumulator of one fused kernel; each tile's winner is folded into a per-row
+ * maximum in the workspace, and the last CTA to finish writes out_idx.
  * By the Gumbel-max identity the result is an exact sample of
  * softmax(l'[b,:]) restricted to the unmasked ids (aitrends.kr write-up,
  * Gumbel-Max paragraph; exactness over tiles because the argmax decomposes
@@ -34,6 +35,13 @@
  * Memory: every pointer in fs_sample_args is a DEVICE pointer owned by the
  * caller; the library allocates no device memory per call.  Calls are
  * asynchronous on the given stream and never synchronise it.
+ *
+ * Workspace: calls that sample (out_idx != NULL) need fs_workspace_size(B, V)
+ * bytes of device workspace that is all-zero before the first call that uses
+ * it (e.g. cudaMemset once after allocating).  Every call returns it to
+ * all-zero, including a call that ends with a device-side timeout, so it can
+ * be reused call after call.  Two calls that may run at the same time (on
+ * different streams) need different workspaces.
  */
 #ifndef FS_SAMPLE_H_
 #define FS_SAMPLE_H_
@@ -83,12 +91,14 @@ typedef struct fs_sample_args {
    * Group-Gumbel-Max paragraphs). */
   int64_t *out_idx;
   /* Optional per-tile outputs, each [B, ceil(V/128)] row-major, or NULL.
-   * out_tile_max and out_tile_idx are either both given or both NULL. */
+   * out_tile_max and out_tile_idx are either both given or both NULL;
+   * out_tile_lse (given => the kernel also computes L_t) needs them. */
   float *out_tile_max;
   int32_t *out_tile_idx;
-  float *out_tile_lse; /* given => the kernel also computes L_t */
-  /* Device scratch of at least fs_workspace_size(B, V) bytes, 256-byte
-   * aligned; needed only when out_tile_max/out_tile_idx are NULL. */
+  float *out_tile_lse;
+  /* Device workspace, 256-byte aligned, at least fs_workspace_size(B, V)
+   * bytes, all-zero before its first use (see "Workspace" above); required
+   * when out_idx is given, ignored otherwise. */
   void *workspace;
   size_t workspace_bytes;
 } fs_sample_args;
@@ -96,13 +106,13 @@ typedef struct fs_sample_args {
 /* Number of 128-wide vocabulary tiles, ceil(V / 128); 0 for V <= 0. */
 int64_t fs_num_tiles(int64_t V);
 
-/* Bytes of workspace fs_sample needs when the caller does not take the
- * per-tile (max, index) outputs: B * ceil(V/128) * 8, rounded up to 256.
- * Returns 0 for non-positive sizes. */
+/* Bytes of workspace a sampling call needs: 256 + 8 * B (a CTA ticket and one
+ * 64-bit running maximum per row), rounded up to 256.  Returns 0 for
+ * non-positive sizes. */
 size_t fs_workspace_size(int64_t B, int64_t V);
 
 /*
- * Sample one token per row (stage 1 + stage 2 above) on `stream` (a
+ * Sample one token per row (the computation above) on `stream` (a
  * cudaStream_t; NULL = the legacy default stream).  Arguments are checked on
  * the host first: on FS_ERR_INVALID_ARG / FS_ERR_WORKSPACE / FS_ERR_UNSUPPORTED
  * nothing is launched and no output is written.  FS_ERR_CUDA reports a failed
@@ -112,8 +122,9 @@ size_t fs_workspace_size(int64_t B, int64_t V);
  */
 fs_status fs_sample(const fs_sample_args *args, void *stream);
 
-/* Size of the library's built-in scratch array used by fs_sample_noalloc. */
-#define FS_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20) /* 8 MiB */
+/* Size of the library's built-in scratch array used by fs_sample_noalloc:
+ * enough for B <= 8160 rows. */
+#define FS_NOALLOC_SCRATCH_BYTES ((size_t)64 << 10) /* 64 KiB */
 
 /*
  * fs_sample for callers that cannot allocate device memory.  (The FlashSampling
@@ -130,17 +141,17 @@ fs_status fs_sample(const fs_sample_args *args, void *stream);
  * owns and passes every input and output.  The library calls no cudaMalloc,
  * cudaFree or other allocating routine on this path.
  *
- * - Limit: when out_tile_max/out_tile_idx are NULL the scratch must hold
- *   fs_workspace_size(B, V) bytes; larger problems return FS_ERR_WORKSPACE
- *   before anything is launched.  With per-tile outputs given no scratch is
- *   used and fs_sample's limits apply.
+ * - Limit: a sampling call (out_idx given) needs fs_workspace_size(B, V) <=
+ *   FS_NOALLOC_SCRATCH_BYTES, i.e. B <= 8160; larger batches return
+ *   FS_ERR_WORKSPACE before anything is launched.  Calls that only write
+ *   per-tile outputs use no scratch.
  * - Set-up: the first call on a device (with that device current) looks up the
- *   array's device address once; make that first call before any stream
+ *   array's device address and clears the array once (a synchronous
+ *   cudaMemset, not an allocation); make that first call before any stream
  *   capture.
- * - Sharing: every call on a device uses the same array, which keeps the last
- *   call's contents (nothing in it needs to start at zero: stage 1 writes
- *   every entry stage 2 reads).  Calls that overlap on the GPU (concurrent
- *   streams) race on it; serialise them.
+ * - Sharing: every call on a device uses the same array.  The array must be
+ *   all-zero when a call starts, and every call leaves it all-zero.  Calls that
+ *   overlap on the GPU (concurrent streams) race on it; serialise them.
  */
 fs_status fs_sample_noalloc(const fs_sample_args *args, void *stream);
 

@@ -121,7 +121,9 @@ def fs_sample(H, W, *, temperature=None, vocab_mask=None, seeds=None, seed=0, of
     H: bf16 [B, d]; W: bf16 [V, d]; temperature: fp32 [B] or None (T = 1);
     vocab_mask: int32 [B, >= ceil(V/32)] allow-bits or None; seeds: int64 [B]
     holding uint64 bit patterns, or None (``seed`` for every row).  Optional
-    per-tile outputs are [B, ceil(V/128)] (fp32 / int32 / fp32).  Returns
+    per-tile outputs are [B, ceil(V/128)] (fp32 / int32 / fp32).  workspace:
+    a uint8 tensor of fs_workspace_size(B, V) bytes that is all-zero before
+    its first use (calls leave it zeroed), or None for a fresh one.  Returns
     ``out_idx`` (int64 [B]).  Asynchronous on ``stream`` (default: the
     current stream of H's device).  With ``reduce=False`` only stage 1 runs:
     the per-tile outputs (required then) are written and None is returned."""
@@ -146,20 +148,16 @@ def fs_sample(H, W, *, temperature=None, vocab_mask=None, seeds=None, seed=0, of
         raise FsError(FS_ERR_INVALID_ARG, "seeds must be int64 (uint64 bit patterns)")
     if temperature is not None and temperature.dtype != torch.float32:
         raise FsError(FS_ERR_INVALID_ARG, "temperature must be float32")
-    ws_bytes = 0
-    if out_tile_max is None:
-        ws_bytes = fs_workspace_size(B, V)
-        if workspace is None:
-            workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    if reduce and workspace is None:  # zero-filled, as the library requires
+        workspace = torch.zeros(fs_workspace_size(B, V), dtype=torch.uint8, device=dev)
     args = FsSampleArgs(
         H=_ptr(H), W=_ptr(W), temperature=_ptr(temperature), vocab_mask=_ptr(vocab_mask),
         mask_ld=mask_ld, seeds=_ptr(seeds), seed=int(seed) & (2**64 - 1),
         offset=int(offset) & (2**64 - 1), B=B, d=d, V=V, ldh=H.stride(0), ldw=W.stride(0),
         out_idx=_ptr(out_idx), out_tile_max=_ptr(out_tile_max), out_tile_idx=_ptr(out_tile_idx),
         out_tile_lse=_ptr(out_tile_lse),
-        workspace=_ptr(workspace) if out_tile_max is None else None,
-        workspace_bytes=(workspace.numel() * workspace.element_size()) if (
-            out_tile_max is None and workspace is not None) else 0)
+        workspace=_ptr(workspace) if reduce else None,
+        workspace_bytes=(workspace.numel() * workspace.element_size()) if reduce else 0)
     with torch.cuda.device(dev):
         st = lib.fs_sample(ctypes.byref(args), _stream_handle(stream, dev))
     if st != FS_OK:

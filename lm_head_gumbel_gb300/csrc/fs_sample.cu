@@ -16,10 +16,11 @@
 //             columns (one output tile); it reads its logits from tensor
 //             memory, scales by 1/T, masks, adds Philox Gumbel noise, and
 //             keeps the running (max, argmax) and optionally the log-sum-exp
-// Only (m_t, i_t[, L_t]) per (row, 128-id tile) is written to device memory.
+// Only (m_t, i_t[, L_t]) per (row, 128-id tile) leaves the chip.
 //
-// Stage 2 ("Stage 2 (Reduction)"): one warp per row reduces its tiles to the
-// sampled id, lowest id on ties.
+// Stage 2 ("Stage 2 (Reduction)") is fused: each tile winner is folded into a
+// per-row 64-bit key with an order-free atomic max, and the last CTA to finish
+// writes the sampled ids (lowest id on ties) and clears the keys.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -68,9 +69,12 @@ struct Stage1Params {
   int64_t mask_ld;
   const uint64_t* seeds;
   uint64_t seed, offset;
-  float* tile_max;
+  float* tile_max;             // per-tile outputs, or null
   int32_t* tile_idx;
   float* tile_lse;
+  int64_t* out_idx;            // sampled ids, or null (per-tile outputs only)
+  unsigned long long* row_keys;  // [B] packed (score, id) maxima, zero between calls
+  uint32_t* ticket;            // CTAs finished so far, wraps back to zero
   uint64_t wait_limit_ns;
   uint32_t h_box_rows;  // rows of the H box: min(128, B rounded up to 8)
 };
@@ -111,6 +115,19 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// (score, id) as one unsigned 64-bit key whose order is: higher score first,
+// then lower id (the tie rule).  The score's bits are mapped to an order-
+// preserving unsigned word (-0 folded into +0); every valid key is nonzero.
+__device__ __forceinline__ unsigned long long pack_key(float m, int32_t idx) {
+  uint32_t b = __float_as_uint(m + 0.0f);
+  b = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return (static_cast<unsigned long long>(b) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(idx));
+}
+
+__device__ __forceinline__ int64_t unpack_idx(unsigned long long key) {
+  return key == 0ull ? int64_t(-1) : int64_t(0xFFFFFFFFu - static_cast<uint32_t>(key));
 }
 
 // One thread, one batch row, one 128-id output tile: read the logits from
@@ -197,6 +214,10 @@ __device__ __forceinline__ void epilogue_tile(const Stage1Params& p, uint32_t ta
     }
   }
   if (!valid_row) return;
+  // Fold the tile's winner into the row's running maximum: the key orders by
+  // score, then by lower id, so the result does not depend on arrival order.
+  if (p.out_idx != nullptr && best_idx >= 0) atomicMax(p.row_keys + row, pack_key(best, best_idx));
+  if (p.tile_max == nullptr) return;
   const int64_t o = int64_t(row) * p.n_tiles + tile;
   p.tile_max[o] = best;
   p.tile_idx[o] = best_idx;
@@ -390,6 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   ptx::tc_fence_before();
+  __threadfence();  // this thread's row-key updates are visible device-wide
   __syncthreads();
   if (warp == 1) {
     ptx::tc_fence_after();
@@ -398,38 +420,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   // No CTA leaves while a peer may still multicast into it or arrive on its
   // barriers.
   if (kCluster > 1) ptx::cluster_sync();
-}
 
-// Stage 2: out_idx[b] = i_t* with t* = argmax_t m_t, lowest id on ties.
-__global__ void __launch_bounds__(256) stage2_kernel(const float* __restrict__ tile_max,
-                                                     const int32_t* __restrict__ tile_idx,
-                                                     int32_t B, int32_t n_tiles,
-                                                     int64_t* __restrict__ out_idx) {
-  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= B) return;
-  const float* m = tile_max + int64_t(row) * n_tiles;
-  const int32_t* ix = tile_idx + int64_t(row) * n_tiles;
-  float best = -INFINITY;
-  int32_t bi = -1;
-  for (int t = lane; t < n_tiles; t += 32) {
-    const int32_t i = ix[t];
-    const float v = m[t];
-    if (i >= 0 && (bi < 0 || v > best)) {
-      best = v;
-      bi = i;
+  // Stage 2 ("Stage 2 (Reduction)"), fused: the last CTA to finish turns the
+  // per-row maxima into sampled ids and clears them for the next call.  The
+  // ticket wraps to zero on the last arrival, so it too is left cleared.
+  if (p.out_idx != nullptr) {
+    __shared__ uint32_t s_is_last;
+    if (threadIdx.x == 0) {
+      __threadfence();
+      s_is_last = (atomicInc(p.ticket, gridDim.x - 1u) == gridDim.x - 1u) ? 1u : 0u;
+    }
+    __syncthreads();
+    if (s_is_last) {
+      __threadfence();
+      for (int r = threadIdx.x; r < p.B; r += blockDim.x)
+        p.out_idx[r] = unpack_idx(atomicExch(p.row_keys + r, 0ull));
     }
   }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    const float ov = __shfl_xor_sync(0xFFFFFFFFu, best, off);
-    const int32_t oi = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
-    if (oi >= 0 && (bi < 0 || ov > best || (ov == best && oi < bi))) {
-      best = ov;
-      bi = oi;
-    }
-  }
-  if (lane == 0) out_idx[row] = bi;
 }
 
 // The noise stage 1 adds, element by element (diagnostic entry point).
@@ -597,9 +604,12 @@ using namespace fs;
 
 extern "C" int64_t fs_num_tiles(int64_t V) { return V <= 0 ? 0 : (V + kTileV - 1) / kTileV; }
 
+// Workspace layout: [0, 4) the CTA ticket, [256, 256 + 8B) the per-row keys.
+constexpr size_t kKeysOffset = 256;
+
 extern "C" size_t fs_workspace_size(int64_t B, int64_t V) {
   if (B <= 0 || V <= 0) return 0;
-  const size_t bytes = size_t(B) * size_t(fs_num_tiles(V)) * 8u;
+  const size_t bytes = kKeysOffset + size_t(B) * 8u;
   return (bytes + 255u) & ~size_t(255u);
 }
 
@@ -632,18 +642,14 @@ extern "C" fs_status fs_sample(const fs_sample_args* a, void* stream_ptr) {
   if ((a->out_tile_max == nullptr) != (a->out_tile_idx == nullptr)) return FS_ERR_INVALID_ARG;
   if (a->out_tile_max && (!aligned(a->out_tile_max, 4) || !aligned(a->out_tile_idx, 4)))
     return FS_ERR_INVALID_ARG;
-  if (a->out_tile_lse && !aligned(a->out_tile_lse, 4)) return FS_ERR_INVALID_ARG;
+  if (a->out_tile_lse && (!aligned(a->out_tile_lse, 4) || !a->out_tile_max))
+    return FS_ERR_INVALID_ARG;
 
   const int64_t n_tiles = fs_num_tiles(V);
-  float* tmax = a->out_tile_max;
-  int32_t* tidx = a->out_tile_idx;
-  if (tmax == nullptr) {
+  if (a->out_idx != nullptr) {
     const size_t need = fs_workspace_size(B, V);
     if (!a->workspace || a->workspace_bytes < need || !aligned(a->workspace, 256))
       return FS_ERR_WORKSPACE;
-    tmax = static_cast<float*>(a->workspace);
-    tidx = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(a->workspace) +
-                                      size_t(B) * size_t(n_tiles) * 4u);
   }
 
   int num_sms = 0;
@@ -680,9 +686,14 @@ extern "C" fs_status fs_sample(const fs_sample_args* a, void* stream_ptr) {
   p.seeds = a->seeds;
   p.seed = a->seed;
   p.offset = a->offset;
-  p.tile_max = tmax;
-  p.tile_idx = tidx;
+  p.tile_max = a->out_tile_max;
+  p.tile_idx = a->out_tile_idx;
   p.tile_lse = a->out_tile_lse;
+  p.out_idx = a->out_idx;
+  p.ticket = a->out_idx ? static_cast<uint32_t*>(a->workspace) : nullptr;
+  p.row_keys = a->out_idx ? reinterpret_cast<unsigned long long*>(
+                                static_cast<uint8_t*>(a->workspace) + kKeysOffset)
+                          : nullptr;
   p.wait_limit_ns = kWaitLimitNs;
   p.h_box_rows = h_rows;
 
@@ -697,19 +708,12 @@ extern "C" fs_status fs_sample(const fs_sample_args* a, void* stream_ptr) {
   else
     lst = lse ? launch_stage1<true, 1>(tmap_h, tmap_w, p, mc, stream)
               : launch_stage1<false, 1>(tmap_h, tmap_w, p, mc, stream);
-  if (lst != FS_OK) return lst;
-
-  if (a->out_idx == nullptr) return FS_OK;  // stage 1 only
-  const int rows_per_block = 256 / 32;
-  stage2_kernel<<<int((B + rows_per_block - 1) / rows_per_block), 256, 0, stream>>>(
-      tmax, tidx, int32_t(B), int32_t(n_tiles), a->out_idx);
-  if (cudaGetLastError() != cudaSuccess) return FS_ERR_CUDA;
-  return FS_OK;
+  return lst;
 }
 
 // ---- allocation-free variant ---------------------------------------------
 // Scratch of fs_sample_noalloc: a file-scope device array, so callers that
-// cannot allocate device memory still have the stage-1 -> stage-2 workspace.
+// cannot allocate device memory still have the per-row reduction workspace.
 // In host code `g_noalloc_scratch` is only a host-side stand-in for the symbol;
 // its device address is looked up once per device with cudaGetSymbolAddress.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[FS_NOALLOC_SCRATCH_BYTES];
@@ -718,8 +722,8 @@ namespace fs {
 namespace {
 void* g_noalloc_addr[kMaxDevices] = {};
 
-// Device address of g_noalloc_scratch on the current device (looked up on the
-// first call per device).
+// Device address of g_noalloc_scratch on the current device (looked up, and
+// the array cleared, on the first call per device).
 fs_status noalloc_scratch(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -729,7 +733,8 @@ fs_status noalloc_scratch(void** out) {
   std::lock_guard<std::mutex> lock(g_mu);
   if (g_noalloc_addr[dev] == nullptr) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr ||
+        cudaMemset(p, 0, FS_NOALLOC_SCRATCH_BYTES) != cudaSuccess) {
       cudaGetLastError();
       return FS_ERR_CUDA;
     }
@@ -743,7 +748,7 @@ fs_status noalloc_scratch(void** out) {
 
 extern "C" fs_status fs_sample_noalloc(const fs_sample_args* a, void* stream_ptr) {
   if (a == nullptr) return FS_ERR_INVALID_ARG;
-  if (a->out_tile_max == nullptr) {  // the built-in scratch must hold the workspace
+  if (a->out_idx != nullptr) {  // the built-in scratch must hold the workspace
     if (a->B < 1 || a->B > 65535 || a->V < 1 || a->V > int64_t(0x7FFFFFFF))
       return FS_ERR_INVALID_ARG;
     if (fs_workspace_size(a->B, a->V) > FS_NOALLOC_SCRATCH_BYTES) return FS_ERR_WORKSPACE;

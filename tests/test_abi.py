@@ -61,9 +61,10 @@ def test_host_helpers(lib):
     assert fs.fs_num_tiles(129) == 2
     assert fs.fs_num_tiles(151936) == 1187
     assert fs.fs_num_tiles(0) == 0
-    assert fs.fs_workspace_size(4, 4096) == 1024
-    assert fs.fs_workspace_size(3, 129) == 256
-    assert fs.fs_workspace_size(512, 151936) == ((512 * 1187 * 8 + 255) // 256) * 256
+    assert fs.fs_workspace_size(4, 4096) == 512
+    assert fs.fs_workspace_size(3, 129) == 512
+    assert fs.fs_workspace_size(512, 151936) == 256 + 512 * 8
+    assert fs.fs_workspace_size(65535, 151936) == ((256 + 65535 * 8 + 255) // 256) * 256
     assert fs.fs_workspace_size(0, 10) == 0
     for code, name in ((0, "FS_OK"), (1, "FS_ERR_INVALID_ARG"), (2, "FS_ERR_UNSUPPORTED"),
                        (3, "FS_ERR_CUDA"), (4, "FS_ERR_DEVICE_TIMEOUT"), (5, "FS_ERR_WORKSPACE")):
@@ -86,8 +87,10 @@ def _args(**kw):
     (dict(H=0x10002), 1), (dict(W=0x20008), 1), (dict(out_idx=0x30004), 1),
     (dict(out_tile_idx=None), 1), (dict(out_tile_max=None), 1),
     (dict(vocab_mask=0x60000, mask_ld=127), 1),
+    (dict(out_tile_lse=0x80000, out_tile_max=None, out_tile_idx=None), 1),
+    (dict(), 5),                                   # sampling without a workspace
     (dict(out_tile_max=None, out_tile_idx=None), 5),
-    (dict(out_tile_max=None, out_tile_idx=None, workspace=0x70000, workspace_bytes=255), 5),
+    (dict(out_tile_max=None, out_tile_idx=None, workspace=0x70000, workspace_bytes=511), 5),
     (dict(out_tile_max=None, out_tile_idx=None, workspace=0x70080, workspace_bytes=4096), 5),
 ])
 def test_bad_arguments_rejected_on_host(lib, kw, want):

@@ -86,7 +86,7 @@ def test_qwen3_8b_head(B):
     steps = 1000 if B <= 64 else 50
     checked = (0, 1, steps // 2, steps - 1)
     out = torch.empty((steps, B), dtype=torch.int64, device="cuda")
-    ws = torch.empty(fs.fs_workspace_size(B, W.shape[0]), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(fs.fs_workspace_size(B, W.shape[0]), dtype=torch.uint8, device="cuda")
     for step in range(steps):
         fs.fs_sample(p["H"], W, temperature=p["temperature"], seeds=p["seeds"], offset=step,
                      out_idx=out[step], workspace=ws)

@@ -117,7 +117,7 @@ def test_graph_replay_matches_eager():
     p = make_problem(8, 64, 3000, T=1.0, seed=8)
     eager = run_device(p, offset=4)["idx"]
     out = torch.empty(8, dtype=torch.int64, device="cuda")
-    ws = torch.empty(fs.fs_workspace_size(8, 3000), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(fs.fs_workspace_size(8, 3000), dtype=torch.uint8, device="cuda")
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
         fs.fs_sample(p["H"], p["W"], temperature=p["temperature"], seed=7, offset=4,
@@ -140,7 +140,7 @@ def test_chi_square_on_device():
     V, d, T, n = 16, 64, 0.8, 6000
     p = make_problem(1, d, V, T=T, seed=12)
     out = torch.empty(1, dtype=torch.int64, device="cuda")
-    ws = torch.empty(fs.fs_workspace_size(1, V), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(fs.fs_workspace_size(1, V), dtype=torch.uint8, device="cuda")
     draws = torch.empty(n, dtype=torch.int64, device="cuda")
     for off in range(n):
         fs.fs_sample(p["H"], p["W"], temperature=p["temperature"], seed=99, offset=off,
