@@ -25,7 +25,7 @@
  * Conventions fixed by this library where the pages are silent:
  *   - uniforms: Philox4x32-10 (Salmon et al., SC'11), key = (seed_b low word,
  *     seed_b high word), counter = (v >> 2, b, offset low word, offset high
- *     word), output word v & 3; u = ((word >> 9) + 0.5) * 2^-23 in (0,1);
+ *     word), output word v & 3; u = ((word & 0x7fffff) + 0.5) * 2^-23 in (0,1);
  *   - T_b <= 0, NaN or +inf selects greedy decoding for row b: s = l, no noise;
  *   - ties go to the lowest vocabulary index, inside a tile and across tiles;
  *   - a fully masked tile reports m = -inf, i = -1, L = -inf; a fully masked

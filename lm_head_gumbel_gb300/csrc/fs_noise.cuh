@@ -47,31 +47,54 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 x, const PhiloxSchedule& ks
   return x;
 }
 
-// Gumbel(0,1) noise from one random word, in fp32.
+// Hardware base-2 logarithm (flush-to-zero form: every argument used here is
+// a normal number, so no subnormal handling is needed).
+__device__ __forceinline__ float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLog2Ln2 = -0.5287663729448977f;  // log2(ln 2)
+
+// The Gumbel noise of one random word, in base-2 units: returns
+// q = log2(-log2 u), so that g = -log(-log u) = -ln2 * (q + log2(ln 2)).
 //
-// u = ((w >> 9) + 1/2) 2^-23: built from the bit pattern 1 + k 2^-23 minus
-// (1 - 2^-24), exact (at most 24 significant bits), so 0 < u < 1; x = 1 - u is
-// exact as well.  Then g = -ln(e) with e = -ln(u):
-//  - the inner log decides the largest noise values (u near 1, e tiny), which
-//    are the ones that win the argmax, so there it must be accurate relative to
-//    e.  For x < 2^-5 it uses the Taylor series of -ln(1 - x) = x (1 + x/2 +
-//    x^2/3 + x^3/4 + x^4/5 + ...), truncated after x^4/5 (relative truncation
-//    error below x^5/6 < 6e-9); otherwise -ln2 * log2(u) with the hardware base-2
-//    logarithm, whose absolute error (< 2^-22 on [1/2, 2]) is then at most
-//    ~5e-6 relative to |log2 u| >= 0.046;
-//  - the outer log only needs absolute accuracy: -ln2 * log2(e).
-// The noise differs from the exact fp64 -log(-log u) by a few 1e-6 at most.
-__device__ __forceinline__ float gumbel_from_word(uint32_t w) {
-  constexpr float kLn2 = 0.693147180559945f;
-  const float f = __uint_as_float(0x3F800000u | (w >> 9));  // 1 + k 2^-23
-  const float u = f - 0x1.fffffep-1f;                        // k 2^-23 + 2^-24
+// u = ((w & 0x7fffff) + 1/2) 2^-23: built from the bit pattern 1 + k 2^-23
+// minus (1 - 2^-24), exact (at most 24 significant bits), so 0 < u < 1;
+// x = 1 - u is exact as well.  Then E = -log2 u:
+//  - E decides the largest noise values (u near 1, E tiny), which are the ones
+//    that win the argmax, so there it must be accurate relative to E.  For
+//    x < 2^-5 it uses the Taylor series -log2(1 - x) = log2(e) (x + x^2/2 +
+//    x^3/3 + x^4/4 + x^5/5 + ...), truncated after x^5/5 (relative truncation
+//    error below x^5/6 < 6e-9); otherwise the hardware log2 of u, whose
+//    absolute error (< 2^-22 on [1/2, 2]) is then at most ~5e-6 relative to
+//    |log2 u| >= 0.046;
+//  - q = log2 E only needs absolute accuracy.
+// The resulting g differs from the exact fp64 -log(-log u) by a few 1e-6.
+__device__ __forceinline__ float gumbel_log2_from_word(uint32_t w) {
+  const float f = __uint_as_float(0x3F800000u | (w & 0x7FFFFFu));  // 1 + k 2^-23
+  const float u = f - 0x1.fffffep-1f;                               // k 2^-23 + 2^-24
   const float x = 1.0f - u;
-  float ser = fmaf(x, 0.2f, 0.25f);
-  ser = fmaf(x, ser, 0.333333343f);
-  ser = fmaf(x, ser, 0.5f);
-  ser = fmaf(x, ser, 1.0f);
-  const float e = (x < 0x1p-5f) ? x * ser : -kLn2 * __log2f(u);
-  return -kLn2 * __log2f(e);
+  float ser = fmaf(x, 0.2f * kLog2e, 0.25f * kLog2e);
+  ser = fmaf(x, ser, kLog2e / 3.0f);
+  ser = fmaf(x, ser, 0.5f * kLog2e);
+  ser = fmaf(x, ser, kLog2e);
+  const float E = (x < 0x1p-5f) ? x * ser : -lg2_approx(u);
+  return lg2_approx(E);
+}
+
+// Gumbel(0,1) noise of one random word, in natural units.
+__device__ __forceinline__ float gumbel_from_word(uint32_t w) {
+  return -kLn2 * (gumbel_log2_from_word(w) + kLog2Ln2);
 }
 
 __device__ __forceinline__ uint32_t select_word(uint4 r, uint32_t which) {

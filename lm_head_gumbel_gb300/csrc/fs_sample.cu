@@ -111,12 +111,6 @@ struct Waiter {
   }
 };
 
-__device__ __forceinline__ float ex2_approx(float x) {
-  float y;
-  asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
 // (score, id) as one unsigned 64-bit key whose order is: higher score first,
 // then lower id (the tie rule).  The score's bits are mapped to an order-
 // preserving unsigned word (-0 folded into +0); every valid key is nonzero.
@@ -130,13 +124,50 @@ __device__ __forceinline__ int64_t unpack_idx(unsigned long long key) {
   return key == 0ull ? int64_t(-1) : int64_t(0xFFFFFFFFu - static_cast<uint32_t>(key));
 }
 
+// One 32-column chunk of a sampling row, in base-2 units: s2 = l * (log2 e / T)
+// - log2(-log2 u), which is s * log2(e) shifted by a constant, so it has the
+// same argmax.  Updates the running maximum `best2` and, if this chunk holds
+// a new maximum, its position `best_j` in the chunk (else leaves -1).
+template <bool kMasked>
+__device__ __forceinline__ void sample_chunk(const uint32_t (&r)[32], uint32_t allow,
+                                             float scale2, uint32_t ctr0, uint32_t ctr_row,
+                                             uint32_t ctr_lo, uint32_t ctr_hi,
+                                             const PhiloxSchedule& ks, float& best2,
+                                             int& best_j) {
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    const uint4 rnd = philox4x32_10(make_uint4(ctr0 + g, ctr_row, ctr_lo, ctr_hi), ks);
+    const uint32_t words[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int j = g * 4 + i;
+      const float s2 = fmaf(__uint_as_float(r[j]), scale2, -gumbel_log2_from_word(words[i]));
+      if ((!kMasked || ((allow >> j) & 1u)) && s2 > best2) {
+        best2 = s2;
+        best_j = j;
+      }
+    }
+  }
+}
+
+template <bool kMasked>
+__device__ __forceinline__ void greedy_chunk(const uint32_t (&r)[32], uint32_t allow,
+                                             float& best, int& best_j) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const float l = __uint_as_float(r[j]);
+    if ((!kMasked || ((allow >> j) & 1u)) && l > best) {
+      best = l;
+      best_j = j;
+    }
+  }
+}
+
 // One thread, one batch row, one 128-id output tile: read the logits from
 // tensor memory 32 columns at a time and reduce them to (m_t, i_t[, L_t]).
-// Scores are s = l * (1/T) + g (one fma); the log-sum-exp is kept in base 2.
 template <bool kWantLse>
 __device__ __forceinline__ void epilogue_tile(const Stage1Params& p, uint32_t taddr, int row,
                                               int tile) {
-  constexpr float kLog2e = 1.4426950408889634f, kLn2 = 0.6931471805599453f;
   const bool valid_row = row < p.B;
   float T = 1.0f;
   uint64_t seed = p.seed;
@@ -147,14 +178,13 @@ __device__ __forceinline__ void epilogue_tile(const Stage1Params& p, uint32_t ta
     if (p.mask) mrow = p.mask + int64_t(row) * p.mask_ld;
   }
   const bool greedy = !(T > 0.0f) || isinf(T);
-  const float inv_t = greedy ? 1.0f : 1.0f / T;
-  const float inv_t_log2e = inv_t * kLog2e;
+  const float scale2 = greedy ? 1.0f : kLog2e / T;  // l -> l' in base-2 units
   const PhiloxSchedule ks(seed);
   const uint32_t ctr_row = static_cast<uint32_t>(row);
-  const uint32_t ctr_off_lo = static_cast<uint32_t>(p.offset);
-  const uint32_t ctr_off_hi = static_cast<uint32_t>(p.offset >> 32);
+  const uint32_t ctr_lo = static_cast<uint32_t>(p.offset);
+  const uint32_t ctr_hi = static_cast<uint32_t>(p.offset >> 32);
 
-  float best = -INFINITY;
+  float best = -INFINITY;  // greedy: max l; sampling: max s2
   int32_t best_idx = -1;
   float run_max = -INFINITY, run_sum = 0.0f;  // base-2 log-sum-exp state
   const int v_tile = tile * kTileV;
@@ -169,61 +199,49 @@ __device__ __forceinline__ void epilogue_tile(const Stage1Params& p, uint32_t ta
     uint32_t allow = mrow ? mrow[v0 >> 5] : 0xFFFFFFFFu;
     const int n_in = p.V - v0;
     if (n_in < 32) allow &= (n_in <= 0) ? 0u : ((1u << n_in) - 1u);
-
-    if (greedy) {  // s = l, no noise; L_t = max l
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float l = __uint_as_float(r[j]);
-        if (((allow >> j) & 1u) && l > best) {
-          best = l;
-          best_idx = v0 + j;
-        }
-      }
-      continue;
+    int best_j = -1;
+    if (greedy) {
+      if (allow == 0xFFFFFFFFu)
+        greedy_chunk<false>(r, allow, best, best_j);
+      else
+        greedy_chunk<true>(r, allow, best, best_j);
+    } else {
+      const uint32_t ctr0 = static_cast<uint32_t>(v0 >> 2);
+      if (allow == 0xFFFFFFFFu)
+        sample_chunk<false>(r, allow, scale2, ctr0, ctr_row, ctr_lo, ctr_hi, ks, best, best_j);
+      else
+        sample_chunk<true>(r, allow, scale2, ctr0, ctr_row, ctr_lo, ctr_hi, ks, best, best_j);
     }
-#pragma unroll
-    for (int g = 0; g < 8; ++g) {
-      const uint4 rnd = philox4x32_10(
-          make_uint4(static_cast<uint32_t>(v0 >> 2) + g, ctr_row, ctr_off_lo, ctr_off_hi), ks);
-      const uint32_t words[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int j = g * 4 + i;
-        const float s = fmaf(__uint_as_float(r[j]), inv_t, gumbel_from_word(words[i]));
-        if (((allow >> j) & 1u) && s > best) {
-          best = s;
-          best_idx = v0 + j;
-        }
-      }
-    }
-    if (kWantLse) {
+    if (best_j >= 0) best_idx = v0 + best_j;
+    if (kWantLse && !greedy) {
       float cm = -INFINITY;
 #pragma unroll
       for (int j = 0; j < 32; ++j)
-        if ((allow >> j) & 1u) cm = fmaxf(cm, __uint_as_float(r[j]) * inv_t_log2e);
+        if ((allow >> j) & 1u) cm = fmaxf(cm, __uint_as_float(r[j]) * scale2);
       if (cm > -INFINITY) {
         const float m_new = fmaxf(run_max, cm);
         float acc = 0.0f;
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-          if ((allow >> j) & 1u)
-            acc += ex2_approx(fmaf(__uint_as_float(r[j]), inv_t_log2e, -m_new));
+          if ((allow >> j) & 1u) acc += ex2_approx(fmaf(__uint_as_float(r[j]), scale2, -m_new));
         run_sum = fmaf(run_sum, ex2_approx(run_max - m_new), acc);
         run_max = m_new;
       }
     }
   }
   if (!valid_row) return;
+  // Back to natural units: s = ln2 * (s2 - log2(ln 2)).
+  const float m = (greedy || best_idx < 0) ? best : kLn2 * (best - kLog2Ln2);
   // Fold the tile's winner into the row's running maximum: the key orders by
   // score, then by lower id, so the result does not depend on arrival order.
-  if (p.out_idx != nullptr && best_idx >= 0) atomicMax(p.row_keys + row, pack_key(best, best_idx));
+  if (p.out_idx != nullptr && best_idx >= 0) atomicMax(p.row_keys + row, pack_key(m, best_idx));
   if (p.tile_max == nullptr) return;
   const int64_t o = int64_t(row) * p.n_tiles + tile;
-  p.tile_max[o] = best;
+  p.tile_max[o] = m;
   p.tile_idx[o] = best_idx;
   if (kWantLse) {
     float L = best;  // greedy rows: the largest unmasked logit
-    if (!greedy) L = run_max > -INFINITY ? (run_max + __log2f(run_sum)) * kLn2 : -INFINITY;
+    if (!greedy) L = run_max > -INFINITY ? (run_max + lg2_approx(run_sum)) * kLn2 : -INFINITY;
     p.tile_lse[o] = L;
   }
 }

@@ -28,7 +28,8 @@
  *     key = (seed_b & 0xffffffff, seed_b >> 32),
  *     counter = (v >> 2, b, offset & 0xffffffff, offset >> 32),
  *     and output word (v & 3);
- *   - u = ((w >> 9) + 0.5) * 2^-23, so 0 < u < 1 and u is exact in fp32;
+ *   - u = ((w & 0x7fffff) + 0.5) * 2^-23 (the word's low 23 bits), so
+ *     0 < u < 1 and u is exact in fp32;
  *   - ties go to the lowest vocabulary index;
  *   - a fully masked tile or row gives m = -inf, index -1, L = -inf;
  *   - for a greedy row L_t is max l over the tile's unmasked entries.
@@ -72,9 +73,9 @@ void fso_philox4x32_10(const uint32_t counter[4], const uint32_t key[2],
   out[0] = x0; out[1] = x1; out[2] = x2; out[3] = x3;
 }
 
-/* 32-bit random word -> uniform in (0,1): keep the top 23 bits, centre. */
+/* 32-bit random word -> uniform in (0,1): keep the low 23 bits, centre. */
 double fso_uniform(uint32_t word) {
-  return ((double)(word >> 9) + 0.5) * (1.0 / 8388608.0); /* 2^-23 */
+  return ((double)(word & 0x7fffffu) + 0.5) * (1.0 / 8388608.0); /* 2^-23 */
 }
 
 /* Gumbel(0,1) by inversion: g = -log(-log u). */

@@ -90,12 +90,12 @@ def pin_philox_kat(o):
 
 
 def pin_uniform_map(o):
-    """u = ((w >> 9) + 1/2) 2^-23: endpoints, bit use, open interval."""
+    """u = ((w & 0x7fffff) + 1/2) 2^-23: endpoints, bit use, open interval."""
     assert o.uniform(0) == 2.0 ** -24
     assert o.uniform(0xFFFFFFFF) == 1.0 - 2.0 ** -24
-    assert o.uniform(0x1FF) == 2.0 ** -24            # low 9 bits unused
-    assert o.uniform(0x200) == 3.0 * 2.0 ** -24
-    assert o.uniform(0x80000000) == 0.5 + 2.0 ** -24
+    assert o.uniform(0xFF800000) == 2.0 ** -24       # top 9 bits unused
+    assert o.uniform(0x1) == 3.0 * 2.0 ** -24
+    assert o.uniform(0x400000) == 0.5 + 2.0 ** -24
     rng = np.random.default_rng(7)
     ws = rng.integers(0, 2 ** 32, size=2000, dtype=np.uint64)
     us = np.array([o.uniform(int(w)) for w in ws])

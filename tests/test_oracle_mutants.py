@@ -25,7 +25,8 @@ MUTANTS = [
     ("philox-bump-first-round", "if (round > 0) {", "if (round >= 0) {", 0),
     ("philox-output-order", "uint32_t n1 = lo1;", "uint32_t n1 = lo0;", 0),
     ("uniform-no-centre", "+ 0.5) * (1.0 / 8388608.0)", "+ 0.0) * (1.0 / 8388608.0)", 0),
-    ("uniform-wrong-bits", "(word >> 9)", "(word >> 8)", 0),
+    ("uniform-wrong-bits", "(word & 0x7fffffu)", "(word & 0xffffffu)", 0),
+    ("uniform-top-bits", "(word & 0x7fffffu)", "(word >> 9)", 0),
     ("gumbel-sign", "return -log(-log(u));", "return log(-log(u));", 0),
     ("gumbel-single-log", "return -log(-log(u));", "return -log(u);", 0),
     ("counter-drops-row", "counter[1] = (uint32_t)b;", "counter[1] = 0;", 0),
