@@ -3,8 +3,11 @@
 // Stage 1 (the aitrends.kr write-up on FlashSampling, "Stage 1 (Fused
 // Kernel)"; tomesphere abstract, "compute logits tile-by-tile on chip, add
 // Gumbel noise, keep only one maximizer per row and per vocabulary tile"):
-// a persistent, warp-specialised kernel.  Each work unit is a 128-row batch
-// block x 256-id vocabulary block of the logits l = H W^T:
+// a persistent, warp-specialised kernel.  For up to 128 rows (and odd numbers
+// of 128-row blocks) each work unit is a 128-row batch block x 256-id
+// vocabulary block of the logits l = H W^T, computed by one CTA; for an even
+// number of batch blocks, CTA pairs compute 256 x 256 units with cta_group::2
+// MMAs (stage1_pair_kernel below).  Single-CTA roles:
 //   warp 0    TMA producer: streams 64-wide K slices of W (256 x 64) and
 //             H (up to 128 x 64) into a 4-stage shared-memory ring (128-byte
 //             swizzle)
@@ -246,6 +249,26 @@ __device__ __forceinline__ void epilogue_tile(const Stage1Params& p, uint32_t ta
   }
 }
 
+// Stage 2 ("Stage 2 (Reduction)"), fused: the last CTA to finish turns the
+// per-row maxima into sampled ids and clears them for the next call.  The
+// ticket wraps to zero on the last arrival, so it too is left cleared.  Called
+// by every thread of every CTA once its work is done (and its row-key updates
+// fenced).
+__device__ __forceinline__ void finish_rows(const Stage1Params& p) {
+  if (p.out_idx == nullptr) return;
+  __shared__ uint32_t s_is_last;
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_is_last = (atomicInc(p.ticket, gridDim.x - 1u) == gridDim.x - 1u) ? 1u : 0u;
+  }
+  __syncthreads();
+  if (s_is_last) {
+    __threadfence();
+    for (int r = threadIdx.x; r < p.B; r += blockDim.x)
+      p.out_idx[r] = unpack_idx(atomicExch(p.row_keys + r, 0ull));
+  }
+}
+
 // Work decomposition: a unit is (vocabulary block vt of 256 ids, batch block mt
 // of 128 rows).  CTAs run in clusters of kCluster along the batch dimension: the
 // CTAs of a cluster take the kCluster batch blocks of one group of one
@@ -439,22 +462,204 @@ __global__ void __launch_bounds__(kThreads, 1)
   // barriers.
   if (kCluster > 1) ptx::cluster_sync();
 
-  // Stage 2 ("Stage 2 (Reduction)"), fused: the last CTA to finish turns the
-  // per-row maxima into sampled ids and clears them for the next call.  The
-  // ticket wraps to zero on the last arrival, so it too is left cleared.
-  if (p.out_idx != nullptr) {
-    __shared__ uint32_t s_is_last;
-    if (threadIdx.x == 0) {
-      __threadfence();
-      s_is_last = (atomicInc(p.ticket, gridDim.x - 1u) == gridDim.x - 1u) ? 1u : 0u;
+  finish_rows(p);
+}
+
+// ---------------------------------------------------------------------------
+// Stage 1 for batches of more than 128 rows: CTA pairs (2-CTA clusters) run
+// M = 256, N = 256, K = 16 MMAs (cta_group::2).  A unit is (vocabulary block vt
+// of 256 ids, pair block mp of 256 batch rows).  CTA r of the pair loads batch
+// rows mp*256 + r*128 .. +127 (its half of A) and vocabulary rows vt*256 +
+// r*128 .. +127 (its half of B) into its own shared memory, 32 KB a stage, so
+// six stages fit; every copy signals the even ("leader") CTA's full barrier.
+// The leader's single MMA thread accumulates into both CTAs' tensor memory
+// (rows r*128.. in CTA r, all 256 columns) and multicasts its commits to both
+// CTAs' barriers.  Each CTA's epilogue reads its own 128 rows; the leader's
+// "tensor memory empty" barrier collects the epilogue warps of both CTAs.
+constexpr int kPairStages = 6;
+constexpr uint32_t kPairSmemA = 128 * kBlockK * 2;  // 16 KB: this CTA's batch rows
+constexpr uint32_t kPairSmemB = 128 * kBlockK * 2;  // 16 KB: this CTA's vocabulary rows
+constexpr uint32_t kPairStageBytes = kPairSmemA + kPairSmemB;
+constexpr size_t kPairBarOffset = size_t(kPairStages) * kPairStageBytes;
+constexpr size_t kPairSmemBytes = 1024 + kPairBarOffset + 256;
+constexpr uint32_t kPairIdesc = ptx::idesc_bf16_f32(2 * kBlockM, kBlockN);
+static_assert(kPairSmemBytes <= 232448, "pair kernel shared memory");
+
+template <bool kWantLse>
+__global__ void __launch_bounds__(kThreads, 1)
+    stage1_pair_kernel(const __grid_constant__ CUtensorMap tmap_h,
+                       const __grid_constant__ CUtensorMap tmap_w, const Stage1Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kPairBarOffset);
+  uint64_t* empty_bar = full_bar + kPairStages;
+  uint64_t* tfull_bar = empty_bar + kPairStages;
+  uint64_t* tempty_bar = tfull_bar + 2;
+  uint64_t* drain_bar = tempty_bar + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  volatile uint32_t* abort_flag = tmem_holder + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int rank = int(ptx::cluster_ctarank());
+  const bool leader = rank == 0;
+  const int pair_id = int(blockIdx.x) >> 1;
+  const int n_pairs = int(gridDim.x) >> 1;
+  const int n_mp = (p.B + 2 * kBlockM - 1) / (2 * kBlockM);
+  const int n_units = ((p.V + kBlockN - 1) / kBlockN) * n_mp;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPairStages; ++s) {
+      ptx::mbar_init(&full_bar[s], 1);
+      ptx::mbar_init(&empty_bar[s], 1);
     }
-    __syncthreads();
-    if (s_is_last) {
-      __threadfence();
-      for (int r = threadIdx.x; r < p.B; r += blockDim.x)
-        p.out_idx[r] = unpack_idx(atomicExch(p.row_keys + r, 0ull));
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&tfull_bar[a], 1);
+      ptx::mbar_init(&tempty_bar[a], 2 * kEpiWarps);
+    }
+    ptx::mbar_init(drain_bar, 1);
+    *abort_flag = 0u;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tmap_h);
+    ptx::prefetch_tmap(&tmap_w);
+  }
+  if (warp == 1) {  // one warp in each CTA of the pair, together
+    ptx::tmem_alloc_pair(tmem_holder, kTmemCols);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();  // both CTAs' barriers exist before either uses the other's
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const Waiter waiter{abort_flag, p.wait_limit_ns};
+
+  if (warp == 0) {
+    // ---------------- TMA producer (both CTAs) ----------------
+    if (lane == 0) {
+      const uint64_t pol_w = n_mp > 1 ? ptx::policy_evict_normal() : ptx::policy_evict_first();
+      const uint64_t pol_h = ptx::policy_evict_last();
+      uint32_t stage = 0, phase = 0, issued = 0;
+      bool ok = true;
+      for (int u = pair_id; ok && u < n_units; u += n_pairs) {
+        const int vt = u / n_mp, mp = u % n_mp;
+        const int k_start = int((uint32_t(vt) * 5u) % uint32_t(p.n_kb));
+        // Rows past the end are read from the last valid row instead (their
+        // accumulator rows / columns are never used), so no box lies wholly
+        // outside its tensor.
+        const int a_y = min(mp * 2 * kBlockM + rank * kBlockM, p.B - 1);
+        const int w_y = min(vt * kBlockN + rank * (kBlockN / 2), p.V - 1);
+        for (int kk = 0; kk < p.n_kb; ++kk) {
+          const int kb = kk + k_start < p.n_kb ? kk + k_start : kk + k_start - p.n_kb;
+          if (!waiter.wait(&empty_bar[stage], phase ^ 1u)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + size_t(stage) * kPairStageBytes;
+          const uint32_t full_addr = ptx::cluster_addr(&full_bar[stage], 0);
+          if (leader) ptx::mbar_arrive_expect_tx(&full_bar[stage], 2 * kPairStageBytes);
+          ptx::tma_load_2d_pair(sa + kPairSmemA, &tmap_w, full_addr, kb * kBlockK, w_y, pol_w);
+          ptx::tma_load_2d_pair(sa, &tmap_h, full_addr, kb * kBlockK, a_y, pol_h);
+          ++issued;
+          if (++stage == kPairStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // The leader's full barriers see both CTAs' copies land; wait for the
+      // last fill of each stage before anything goes away.
+      if (leader) {
+        for (uint32_t s = 0; s < uint32_t(kPairStages); ++s) {
+          const uint32_t fills = issued / kPairStages + (s < issued % kPairStages ? 1u : 0u);
+          if (fills) waiter.drain(&full_bar[s], (fills - 1u) & 1u);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (leader CTA only) ----------------
+    if (lane == 0 && leader) {
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int u = pair_id; ok && u < n_units; u += n_pairs) {
+        if (!waiter.wait(&tempty_bar[acc], acc_phase ^ 1u)) break;
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * kBlockN;
+        for (int kb = 0; kb < p.n_kb; ++kb) {
+          if (!waiter.wait(&full_bar[stage], phase)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t sa = ptx::smem_u32(smem + size_t(stage) * kPairStageBytes);
+          const uint32_t sb = sa + kPairSmemA;
+#pragma unroll
+          for (int k = 0; k < kBlockK / kUmmaK; ++k) {
+            ptx::mma_bf16_pair(d_tmem, ptx::smem_desc_sw128(sa + k * kUmmaK * 2),
+                               ptx::smem_desc_sw128(sb + k * kUmmaK * 2), kPairIdesc,
+                               (kb | k) != 0 ? 1u : 0u);
+          }
+          ptx::mma_commit_pair_multicast(&empty_bar[stage], 0x3);
+          if (++stage == kPairStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit_pair_multicast(&tfull_bar[acc], 0x3);
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      ptx::mma_commit_pair(drain_bar);
+      waiter.drain(drain_bar, 0);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue (both CTAs) ----------------
+    const int e = warp - 2;
+    const int quad = warp & 3;
+    const int half = e >> 2;
+    const uint32_t tempty_addr0 = ptx::cluster_addr(&tempty_bar[0], 0);
+    const uint32_t tempty_addr1 = ptx::cluster_addr(&tempty_bar[1], 0);
+    uint32_t acc = 0, acc_phase = 0;
+    for (int u = pair_id; u < n_units; u += n_pairs) {
+      const int vt = u / n_mp, mp = u % n_mp;
+      int ok = 0;
+      if (lane == 0) ok = waiter.wait(&tfull_bar[acc], acc_phase) ? 1 : 0;
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const int row0 = mp * 2 * kBlockM + rank * kBlockM + quad * 32;
+      const int tile = vt * 2 + half;
+      if (row0 < p.B && tile < p.n_tiles) {
+        const uint32_t taddr =
+            tmem_base + (uint32_t(quad * 32) << 16) + acc * kBlockN + uint32_t(half * kTileV);
+        epilogue_tile<kWantLse>(p, taddr, row0 + lane, tile);
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_cluster(acc == 0 ? tempty_addr0 : tempty_addr1);
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
     }
   }
+
+  ptx::tc_fence_before();
+  __threadfence();
+  __syncthreads();
+  // Both CTAs are done with each other's barriers and the leader's MMAs have
+  // drained before the pair's tensor memory is released.
+  ptx::cluster_sync();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+  ptx::cluster_sync();
+  finish_rows(p);
 }
 
 // The noise stage 1 adds, element by element (diagnostic entry point).
@@ -488,6 +693,7 @@ struct DeviceState {
   fs_status status = FS_ERR_UNSUPPORTED;
   int num_sms = 0;
   int max_clusters[2][3] = {};  // [want_lse][log2 cluster size]: co-resident clusters
+  int max_pairs[2] = {};        // [want_lse]: co-resident CTA pairs of the pair kernel
 };
 
 std::mutex g_mu;
@@ -498,10 +704,11 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 constexpr int log2_cluster(int c) { return c == 1 ? 0 : c == 2 ? 1 : 2; }
 
-cudaLaunchConfig_t launch_config(int cluster, cudaLaunchAttribute* attr, cudaStream_t stream) {
+cudaLaunchConfig_t launch_config(int cluster, cudaLaunchAttribute* attr, cudaStream_t stream,
+                                 size_t smem = kSmemBytes) {
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = unsigned(cluster);
@@ -532,6 +739,37 @@ bool prepare_variant(DeviceState& st, int sms) {
   }
   st.max_clusters[kWantLse ? 1 : 0][log2_cluster(kCluster)] = n;
   return true;
+}
+
+template <bool kWantLse>
+bool prepare_pair_variant(DeviceState& st, int sms) {
+  auto kern = stage1_pair_kernel<kWantLse>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(kPairSmemBytes)) != cudaSuccess)
+    return false;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = launch_config(2, attr, nullptr, kPairSmemBytes);
+  cfg.gridDim = dim3(unsigned((sms / 2) * 2), 1, 1);
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) return false;
+  st.max_pairs[kWantLse ? 1 : 0] = n;
+  return true;
+}
+
+template <bool kWantLse>
+fs_status launch_stage1_pair(const CUtensorMap& tmap_h, const CUtensorMap& tmap_w,
+                             const Stage1Params& p, int max_pairs, cudaStream_t stream) {
+  const int n_units = int((int64_t(p.V) + kBlockN - 1) / kBlockN) *
+                      int((int64_t(p.B) + 2 * kBlockM - 1) / (2 * kBlockM));
+  const int pairs = n_units < max_pairs ? n_units : max_pairs;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = launch_config(2, attr, stream, kPairSmemBytes);
+  cfg.gridDim = dim3(unsigned(pairs * 2), 1, 1);
+  if (cudaLaunchKernelEx(&cfg, stage1_pair_kernel<kWantLse>, tmap_h, tmap_w, p) != cudaSuccess) {
+    cudaGetLastError();
+    return FS_ERR_CUDA;
+  }
+  return FS_OK;
 }
 
 template <bool kWantLse, int kCluster>
@@ -574,7 +812,8 @@ fs_status device_setup(int* num_sms) {
       st.status = FS_OK;
       if (!prepare_variant<false, 1>(st, sms) || !prepare_variant<true, 1>(st, sms) ||
           !prepare_variant<false, 2>(st, sms) || !prepare_variant<true, 2>(st, sms) ||
-          !prepare_variant<false, 4>(st, sms) || !prepare_variant<true, 4>(st, sms)) {
+          !prepare_variant<false, 4>(st, sms) || !prepare_variant<true, 4>(st, sms) ||
+          !prepare_pair_variant<false>(st, sms) || !prepare_pair_variant<true>(st, sms)) {
         cudaGetLastError();
         st.status = FS_ERR_CUDA;
       }
@@ -679,14 +918,18 @@ extern "C" fs_status fs_sample(const fs_sample_args* a, void* stream_ptr) {
   // that are never read.
   const uint32_t h_rows = B >= kBlockM ? uint32_t(kBlockM) : uint32_t((B + 7) / 8 * 8);
   const int n_mt = int((B + kBlockM - 1) / kBlockM);
-  // Clusters of 2 CTAs along the batch share (multicast) the W slice; used when
-  // the batch blocks pair up exactly.
-  const int cluster = (n_mt % 2 == 0) ? 2 : 1;
+  // An even number of 128-row batch blocks: CTA pairs with M = 256 MMAs, each
+  // CTA holding half of the W slice (six 32 KB stages).  Otherwise single CTAs
+  // with M = 128 and the whole slice (four 48 KB stages); with an odd number of
+  // batch blocks above one, clusters of two CTAs would leave half a pair idle,
+  // so those stay single too.
+  const bool pair = n_mt > 1 && n_mt % 2 == 0;
+  const int cluster = 1;
   CUtensorMap tmap_h, tmap_w;
   if (!encode_2d(&tmap_h, a->H, uint64_t(d), uint64_t(B), uint64_t(a->ldh) * 2u, kBlockK,
                  h_rows) ||
       !encode_2d(&tmap_w, a->W, uint64_t(d), uint64_t(V), uint64_t(a->ldw) * 2u, kBlockK,
-                 uint32_t(kBlockN / cluster)))
+                 uint32_t(pair ? kBlockN / 2 : kBlockN / cluster)))
     return FS_ERR_INVALID_ARG;
 
   Stage1Params p;
@@ -720,7 +963,10 @@ extern "C" fs_status fs_sample(const fs_sample_args* a, void* stream_ptr) {
   const bool lse = a->out_tile_lse != nullptr;
   const int mc = ds.max_clusters[lse ? 1 : 0][log2_cluster(cluster)];
   fs_status lst;
-  if (cluster == 2)
+  if (pair)
+    lst = lse ? launch_stage1_pair<true>(tmap_h, tmap_w, p, ds.max_pairs[1], stream)
+              : launch_stage1_pair<false>(tmap_h, tmap_w, p, ds.max_pairs[0], stream);
+  else if (cluster == 2)
     lst = lse ? launch_stage1<true, 2>(tmap_h, tmap_w, p, mc, stream)
               : launch_stage1<false, 2>(tmap_h, tmap_w, p, mc, stream);
   else
