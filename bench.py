@@ -190,6 +190,30 @@ def dist_init(backend):
     return world, rank, local
 
 
+def barrier(world, device=None):
+    """Everything queued on `device` is done and every rank got here."""
+    import torch
+    cuda = device is not None and torch.device(device).type == "cuda"
+    if cuda:
+        torch.cuda.synchronize(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    if cuda:
+        torch.cuda.synchronize(device)
+
+
+def max_over_ranks(x, world, device="cpu"):
+    """The largest value of x over all ranks (timing: the slowest rank)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def make_inputs(wl_name, B, device):
     import torch
     from lm_head_gumbel_gb300 import workloads as wl
@@ -235,61 +259,18 @@ def run_ours(args):
                      vocab_mask=inp["vocab_mask"], offset=base + k, out_idx=out, workspace=ws,
                      stream=stream)
 
-    def barrier():
-        torch.cuda.synchronize()
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
-        torch.cuda.synchronize()
-
-    def max_over_ranks(x):
-        if world == 1:
-            return x
-        import torch.distributed as dist
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
-
     clocks = ClockSampler(local)
     clocks.start()
     for k in range(max(args.warmup, 3)):
         call(k)
-    barrier()
+    barrier(world, dev)
     t_wall0 = time.time()
     ms = time_calls(lambda k: call(k, args.warmup), args.steps, stream)
     t_wall1 = time.time()
-    barrier()
-    ms = max_over_ranks(ms)
+    barrier(world, dev)
+    ms = max_over_ranks(ms, world, dev)
     us_call = ms * 1000.0 / args.steps
 
-
-    # end to end through the public API: pinned host inputs in, result out
-    Hh = inp["H"].cpu().pin_memory()
-    Th = inp["temperature"].cpu().pin_memory()
-    Sh = inp["seeds"].cpu().pin_memory() if inp["seeds"] is not None else None
-    out_h = torch.empty(B, dtype=torch.int64).pin_memory()
-    Hd = torch.empty_like(inp["H"])
-    Td = torch.empty_like(inp["temperature"])
-    Sd = torch.empty_like(inp["seeds"]) if Sh is not None else None
-
-    def e2e_step(k):
-        Hd.copy_(Hh, non_blocking=True)
-        Td.copy_(Th, non_blocking=True)
-        if Sd is not None:
-            Sd.copy_(Sh, non_blocking=True)
-        fs.fs_sample(Hd, inp["W"], temperature=Td, seeds=Sd, vocab_mask=inp["vocab_mask"],
-                     offset=k, out_idx=out, workspace=ws, stream=stream)
-        out_h.copy_(out, non_blocking=True)
-        stream.synchronize()  # the sampled ids feed the next decode step
-
-    for k in range(3):
-        e2e_step(k)
-    barrier()
-    e2e_steps = max(10, min(args.steps, 500))
-    ms_e2e = max_over_ranks(time_calls(e2e_step, e2e_steps, stream))
-    us_e2e = ms_e2e * 1000.0 / e2e_steps
-    h2d = Hh.numel() * Hh.element_size() + Th.numel() * 4 + (Sh.numel() * 8 if Sh is not None else 0)
-    d2h = out_h.numel() * 8
 
     # batch sweep of the same head (same run, same W)
     sweep = []
@@ -315,6 +296,34 @@ def run_ours(args):
                           "achieved": rf["achieved"], "unit": rf["unit"], "frac": rf["frac"],
                           "window": (ts0, time.time())})
             del inp2, o2, ws2
+    # end to end through the public API: pinned host inputs in, result out
+    Hh = inp["H"].cpu().pin_memory()
+    Th = inp["temperature"].cpu().pin_memory()
+    Sh = inp["seeds"].cpu().pin_memory() if inp["seeds"] is not None else None
+    out_h = torch.empty(B, dtype=torch.int64).pin_memory()
+    Hd = torch.empty_like(inp["H"])
+    Td = torch.empty_like(inp["temperature"])
+    Sd = torch.empty_like(inp["seeds"]) if Sh is not None else None
+
+    def e2e_step(k):
+        Hd.copy_(Hh, non_blocking=True)
+        Td.copy_(Th, non_blocking=True)
+        if Sd is not None:
+            Sd.copy_(Sh, non_blocking=True)
+        fs.fs_sample(Hd, inp["W"], temperature=Td, seeds=Sd, vocab_mask=inp["vocab_mask"],
+                     offset=k, out_idx=out, workspace=ws, stream=stream)
+        out_h.copy_(out, non_blocking=True)
+        stream.synchronize()  # the sampled ids feed the next decode step
+
+    for k in range(3):
+        e2e_step(k)
+    barrier(world, dev)
+    e2e_steps = max(10, min(args.steps, 500))
+    ms_e2e = max_over_ranks(time_calls(e2e_step, e2e_steps, stream), world, dev)
+    us_e2e = ms_e2e * 1000.0 / e2e_steps
+    h2d = Hh.numel() * Hh.element_size() + Th.numel() * 4 + (Sh.numel() * 8 if Sh is not None else 0)
+    d2h = out_h.numel() * 8
+
     clock_rows = clocks.stop()
     for ent in sweep:  # clocks seen while each batch size ran
         c = ClockSampler.summarize(clock_rows, *ent.pop("window"))

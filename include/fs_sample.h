@@ -167,6 +167,16 @@ fs_status fs_gumbel_noise(const uint64_t *seeds, uint64_t seed, uint64_t offset,
                           float *out, void *stream);
 
 /*
+ * Diagnostic: run the sampling kernels' bounded wait on a barrier that nothing
+ * ever arrives on, giving up after limit_ns (1e3 <= limit_ns <= 1e9).  The
+ * kernel records the timeout in the device error word and returns, exactly as
+ * a stalled sampling pipeline would, so a caller can check that timeouts are
+ * reported (fs_last_device_error) and that the context stays usable, without
+ * faulting or hanging the GPU.  FS_ERR_INVALID_ARG for a limit out of range.
+ */
+fs_status fs_wait_timeout_selftest(uint64_t limit_ns, void *stream);
+
+/*
  * Read and clear the device-side error word of the current device (this
  * synchronises the device).  *code receives the raw word (0 = none; bit 0: a
  * bounded pipeline wait timed out).  Returns FS_ERR_DEVICE_TIMEOUT if a wait

@@ -69,6 +69,8 @@ def load_library(path: str = LIB_PATH):
     lib.fs_gumbel_noise.argtypes = [_c_ptr, _c_u64, _c_u64, _c_i64, _c_i64, _c_i64, _c_i64,
                                     _c_ptr, _c_ptr]
     lib.fs_gumbel_noise.restype = ctypes.c_int
+    lib.fs_wait_timeout_selftest.argtypes = [_c_u64, _c_ptr]
+    lib.fs_wait_timeout_selftest.restype = ctypes.c_int
     lib.fs_last_device_error.argtypes = [ctypes.POINTER(ctypes.c_int)]
     lib.fs_last_device_error.restype = ctypes.c_int
     lib.fs_status_string.argtypes = [ctypes.c_int]
@@ -106,6 +108,17 @@ def fs_last_device_error():
     code = ctypes.c_int(0)
     st = load_library().fs_last_device_error(ctypes.byref(code))
     return int(st), int(code.value)
+
+
+def fs_wait_timeout_selftest(limit_ns: int, device=None, stream=None):
+    """Run the kernels' bounded wait on a barrier nothing arrives on (see the
+    header); the timeout then shows in fs_last_device_error()."""
+    lib = load_library()
+    device = torch.device(device or "cuda")
+    with torch.cuda.device(device):
+        st = lib.fs_wait_timeout_selftest(int(limit_ns), _stream_handle(stream, device))
+    if st != FS_OK:
+        raise FsError(st, "fs_wait_timeout_selftest")
 
 
 def _check_2d(name, t, dtype):

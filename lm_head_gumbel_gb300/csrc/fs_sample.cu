@@ -662,6 +662,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   finish_rows(p);
 }
 
+// Diagnostic: the bounded wait of the sampling kernels, on an mbarrier that no
+// thread ever arrives on.  It gives up after limit_ns, records the timeout in
+// the device error word, and returns -- the path a stalled pipeline takes.
+__global__ void wait_timeout_kernel(uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ uint32_t abort_word;
+  ptx::mbar_init(&bar, 1);
+  abort_word = 0u;
+  ptx::fence_barrier_init();
+  const Waiter waiter{&abort_word, limit_ns};
+  waiter.wait(&bar, 0);  // phase 0 never completes
+}
+
 // The noise stage 1 adds, element by element (diagnostic entry point).
 __global__ void noise_kernel(const uint64_t* __restrict__ seeds, uint64_t seed, uint64_t offset,
                              int64_t b0, int64_t nb, int64_t v0, int64_t nv,
@@ -1044,6 +1057,15 @@ extern "C" fs_status fs_gumbel_noise(const uint64_t* seeds, uint64_t seed, uint6
   if (blocks > int64_t(0x7FFFFFFF)) return FS_ERR_INVALID_ARG;
   noise_kernel<<<unsigned(blocks), threads, 0, static_cast<cudaStream_t>(stream_ptr)>>>(
       seeds, seed, offset, b0, nb, v0, nv, out);
+  return cudaGetLastError() == cudaSuccess ? FS_OK : FS_ERR_CUDA;
+}
+
+extern "C" fs_status fs_wait_timeout_selftest(uint64_t limit_ns, void* stream_ptr) {
+  if (limit_ns < 1000u || limit_ns > 1000000000u) return FS_ERR_INVALID_ARG;
+  int num_sms = 0;
+  const fs_status st = device_setup(&num_sms);
+  if (st != FS_OK) return st;
+  wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream_ptr)>>>(limit_ns);
   return cudaGetLastError() == cudaSuccess ? FS_OK : FS_ERR_CUDA;
 }
 
