@@ -101,6 +101,20 @@ typedef struct fs_sample_args {
    * when out_idx is given, ignored otherwise. */
   void *workspace;
   size_t workspace_bytes;
+  /* Global vocabulary id of W's first row (a multiple of 4, >= 0, with
+   * vocab_offset + V < 2^31): a call on a shard of the vocabulary reports
+   * global ids (out_idx, out_tile_idx) and draws the noise of the global ids,
+   * so the exact merge of the shards' samples (fs_group_merge) is the sample of
+   * the unsharded call.  0 for an unsharded call. */
+  int64_t vocab_offset;
+  /* Optional fp32 [B]: the row's largest noisy score m = max_v s[b,v]
+   * (-inf for a fully masked row); needs out_idx. */
+  float *out_max;
+  /* Optional fp32 [B]: the row's log-mass L = log sum exp(l'[b,v]) over the
+   * call's unmasked ids (the group log-mass L_k of the aitrends.kr write-up's
+   * tensor-parallel and Group-Gumbel-Max paragraphs; the largest logit for a
+   * greedy row); needs out_tile_lse.  Adds a small second kernel. */
+  float *out_lse;
 } fs_sample_args;
 
 /* Number of 128-wide vocabulary tiles, ceil(V / 128); 0 for V <= 0. */
@@ -154,6 +168,48 @@ fs_status fs_sample(const fs_sample_args *args, void *stream);
  *   overlap on the GPU (concurrent streams) race on it; serialise them.
  */
 fs_status fs_sample_noalloc(const fs_sample_args *args, void *stream);
+
+/* Merge rules of fs_group_merge. */
+#define FS_MERGE_EXACT 0        /* argmax_k m_k: the sample of the union       */
+#define FS_MERGE_GROUP_GUMBEL 1 /* argmax_k L_k + G_k with fresh Gumbel noise  */
+
+/*
+ * Combine per-partition results into one sample per row (aitrends.kr
+ * write-up, tensor-parallel and Group-Gumbel-Max paragraphs; tomesphere
+ * abstract: exact because argmax decomposes over partitions, grouped variants
+ * exact by hierarchical factorisation).  Inputs are [P, B] row-major (the
+ * partition's outputs one after another): z (int64 sampled global ids, -1 for
+ * a fully masked row), m (fp32 maxima, for FS_MERGE_EXACT), L (fp32
+ * log-masses, for FS_MERGE_GROUP_GUMBEL).
+ *   FS_MERGE_EXACT:        out_idx[b] = z[k*, b], k* = argmax_k m[k, b] (lowest
+ *                          k on ties); equals the unsharded sample when the
+ *                          partitions were sampled with matching vocab_offset,
+ *                          seeds and offset.
+ *   FS_MERGE_GROUP_GUMBEL: k* = argmax_k (L[k, b] + G[k, b]), G Gumbel noise
+ *                          independent of the partitions' own (Philox with the
+ *                          row's seed, counter (k >> 2, b | 2^31, offset low,
+ *                          offset high), word k & 3); out_idx[b] = z[k*, b].
+ * Partitions with z < 0 or L = -inf are skipped; a row with none left gives -1.
+ * out_L (optional, fp32 [B]) = log sum_k exp(L[k, b]) (needs L).  seeds: uint64
+ * [B] or NULL for `seed`.  Device pointers; asynchronous on `stream`.
+ */
+fs_status fs_group_merge(const int64_t *z, const float *m, const float *L, int64_t P,
+                         int64_t B, int mode, const uint64_t *seeds, uint64_t seed,
+                         uint64_t offset, int64_t *out_idx, float *out_L, void *stream);
+
+/*
+ * The online form of the Group-Gumbel-Max merge (aitrends.kr write-up: binary
+ * merge rule with O(1) state): fold the group `step` (new_z, new_L, [B]) into
+ * the running state (state_z, state_L, [B], updated in place; start from
+ * z = -1, L = -inf):  L' = logaddexp(L, new_L); with probability
+ * exp(new_L - L') the state's sample becomes new_z; L <- L'.  The Bernoulli
+ * uniform is the one fs_group_merge uses for partition k = step.  Groups with
+ * new_z < 0 or new_L = -inf leave the state unchanged.
+ */
+fs_status fs_online_merge(int64_t *state_z, float *state_L, const int64_t *new_z,
+                          const float *new_L, int64_t B, uint64_t step,
+                          const uint64_t *seeds, uint64_t seed, uint64_t offset,
+                          void *stream);
 
 /*
  * Diagnostic: the Gumbel noise g[b, v] the stage-1 kernel adds, for rows

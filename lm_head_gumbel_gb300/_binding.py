@@ -21,6 +21,8 @@ FS_ERR_UNSUPPORTED = 2
 FS_ERR_CUDA = 3
 FS_ERR_DEVICE_TIMEOUT = 4
 FS_ERR_WORKSPACE = 5
+FS_MERGE_EXACT = 0
+FS_MERGE_GROUP_GUMBEL = 1
 
 _c_i64 = ctypes.c_int64
 _c_u64 = ctypes.c_uint64
@@ -43,6 +45,7 @@ class FsSampleArgs(ctypes.Structure):
         ("B", _c_i64), ("d", _c_i64), ("V", _c_i64), ("ldh", _c_i64), ("ldw", _c_i64),
         ("out_idx", _c_ptr), ("out_tile_max", _c_ptr), ("out_tile_idx", _c_ptr),
         ("out_tile_lse", _c_ptr), ("workspace", _c_ptr), ("workspace_bytes", ctypes.c_size_t),
+        ("vocab_offset", _c_i64), ("out_max", _c_ptr), ("out_lse", _c_ptr),
     ]
 
 
@@ -69,6 +72,12 @@ def load_library(path: str = LIB_PATH):
     lib.fs_gumbel_noise.argtypes = [_c_ptr, _c_u64, _c_u64, _c_i64, _c_i64, _c_i64, _c_i64,
                                     _c_ptr, _c_ptr]
     lib.fs_gumbel_noise.restype = ctypes.c_int
+    lib.fs_group_merge.argtypes = [_c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, ctypes.c_int, _c_ptr,
+                                   _c_u64, _c_u64, _c_ptr, _c_ptr, _c_ptr]
+    lib.fs_group_merge.restype = ctypes.c_int
+    lib.fs_online_merge.argtypes = [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_i64, _c_u64, _c_ptr, _c_u64,
+                                    _c_u64, _c_ptr]
+    lib.fs_online_merge.restype = ctypes.c_int
     lib.fs_wait_timeout_selftest.argtypes = [_c_u64, _c_ptr]
     lib.fs_wait_timeout_selftest.restype = ctypes.c_int
     lib.fs_last_device_error.argtypes = [ctypes.POINTER(ctypes.c_int)]
@@ -128,7 +137,8 @@ def _check_2d(name, t, dtype):
 
 def fs_sample(H, W, *, temperature=None, vocab_mask=None, seeds=None, seed=0, offset=0,
               out_idx=None, out_tile_max=None, out_tile_idx=None, out_tile_lse=None,
-              workspace=None, stream=None, reduce=True):
+              workspace=None, stream=None, reduce=True, vocab_offset=0, out_max=None,
+              out_lse=None):
     """Sample one token id per row of H from softmax(H W^T / T) (masked).
 
     H: bf16 [B, d]; W: bf16 [V, d]; temperature: fp32 [B] or None (T = 1);
@@ -139,7 +149,10 @@ def fs_sample(H, W, *, temperature=None, vocab_mask=None, seeds=None, seed=0, of
     its first use (calls leave it zeroed), or None for a fresh one.  Returns
     ``out_idx`` (int64 [B]).  Asynchronous on ``stream`` (default: the
     current stream of H's device).  With ``reduce=False`` only stage 1 runs:
-    the per-tile outputs (required then) are written and None is returned."""
+    the per-tile outputs (required then) are written and None is returned.
+    vocab_offset: global id of W's first row (W a vocabulary shard); out_max /
+    out_lse: optional fp32 [B] row maximum / row log-mass (out_lse needs
+    out_tile_lse)."""
     lib = load_library()
     _check_2d("H", H, torch.bfloat16)
     _check_2d("W", W, torch.bfloat16)
@@ -170,12 +183,47 @@ def fs_sample(H, W, *, temperature=None, vocab_mask=None, seeds=None, seed=0, of
         out_idx=_ptr(out_idx), out_tile_max=_ptr(out_tile_max), out_tile_idx=_ptr(out_tile_idx),
         out_tile_lse=_ptr(out_tile_lse),
         workspace=_ptr(workspace) if reduce else None,
-        workspace_bytes=(workspace.numel() * workspace.element_size()) if reduce else 0)
+        workspace_bytes=(workspace.numel() * workspace.element_size()) if reduce else 0,
+        vocab_offset=int(vocab_offset), out_max=_ptr(out_max), out_lse=_ptr(out_lse))
     with torch.cuda.device(dev):
         st = lib.fs_sample(ctypes.byref(args), _stream_handle(stream, dev))
     if st != FS_OK:
         raise FsError(st, "fs_sample")
     return out_idx
+
+
+def fs_group_merge(z, *, m=None, L=None, mode=FS_MERGE_EXACT, seeds=None, seed=0, offset=0,
+                   out_idx=None, out_L=None, stream=None):
+    """One sample per row from P partitions' results z / m / L ([P, B]).
+    mode FS_MERGE_EXACT: argmax of m; FS_MERGE_GROUP_GUMBEL: Group-Gumbel-Max
+    over L with the merge's own noise.  Returns out_idx (int64 [B])."""
+    lib = load_library()
+    P, B = z.shape
+    dev = z.device
+    if out_idx is None:
+        out_idx = torch.empty(B, dtype=torch.int64, device=dev)
+    with torch.cuda.device(dev):
+        st = lib.fs_group_merge(_ptr(z), _ptr(m), _ptr(L), P, B, int(mode), _ptr(seeds),
+                                int(seed) & (2**64 - 1), int(offset) & (2**64 - 1),
+                                _ptr(out_idx), _ptr(out_L), _stream_handle(stream, dev))
+    if st != FS_OK:
+        raise FsError(st, "fs_group_merge")
+    return out_idx
+
+
+def fs_online_merge(state_z, state_L, new_z, new_L, step, *, seeds=None, seed=0, offset=0,
+                    stream=None):
+    """Fold group `step` (new_z, new_L: [B]) into the running (state_z,
+    state_L) in place (start from -1 / -inf)."""
+    lib = load_library()
+    B = state_z.shape[0]
+    dev = state_z.device
+    with torch.cuda.device(dev):
+        st = lib.fs_online_merge(_ptr(state_z), _ptr(state_L), _ptr(new_z), _ptr(new_L), B,
+                                 int(step), _ptr(seeds), int(seed) & (2**64 - 1),
+                                 int(offset) & (2**64 - 1), _stream_handle(stream, dev))
+    if st != FS_OK:
+        raise FsError(st, "fs_online_merge")
 
 
 def fs_gumbel_noise(b0, nb, v0, nv, *, seed=0, offset=0, seeds=None, out=None, device=None,

@@ -1,0 +1,192 @@
+// fs_merge.cu -- combining per-partition sampling results.
+//
+// FlashSampling's exactness arguments (tomesphere abstract: the kernel is exact
+// because argmax decomposes over partitions; grouped variants for online and
+// tensor-parallel settings are exact by hierarchical factorisation of the
+// categorical; aitrends.kr write-up, tensor-parallel and Group-Gumbel-Max
+// paragraphs) turn into three small kernels:
+//   row_lse_kernel      the row's log-mass L = log sum_t exp(L_t) from the
+//                       stage-1 kernel's per-tile log-masses;
+//   group_merge_kernel  one sample per row from P partitions' (z_k, m_k, L_k):
+//                       exact (argmax_k m_k) or Group-Gumbel-Max
+//                       (argmax_k L_k + G_k, fresh Gumbel noise);
+//   online_merge_kernel the O(1)-state binary merge rule with a Bernoulli
+//                       switch, one group at a time.
+// The merges' own randomness uses Philox on a counter domain the sampling noise
+// never uses (second counter word = row | 2^31), keyed by the row's seed.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "fs_noise.cuh"
+#include "fs_sample.h"
+
+namespace fs {
+namespace {
+
+constexpr int kLseThreads = 128;
+constexpr int kMergeThreads = 128;
+
+__device__ __forceinline__ float block_reduce(float v, bool is_max) {
+  __shared__ float part[kLseThreads / 32];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float o = __shfl_xor_sync(0xFFFFFFFFu, v, off);
+    v = is_max ? fmaxf(v, o) : v + o;
+  }
+  __syncthreads();  // part[] may still be read by a previous call
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float r = part[0];
+#pragma unroll
+  for (int w = 1; w < kLseThreads / 32; ++w) r = is_max ? fmaxf(r, part[w]) : r + part[w];
+  return r;
+}
+
+// One block per row.  Greedy rows (T <= 0, NaN or inf) report the largest
+// tile value, i.e. the row's largest logit, matching the per-tile convention.
+__global__ void __launch_bounds__(kLseThreads)
+    row_lse_kernel(const float* __restrict__ tile_lse, const float* __restrict__ temperature,
+                   int32_t n_tiles, float* __restrict__ out_lse) {
+  const int row = blockIdx.x;
+  const float* t = tile_lse + int64_t(row) * n_tiles;
+  float m = -INFINITY;
+  for (int i = threadIdx.x; i < n_tiles; i += kLseThreads) m = fmaxf(m, t[i]);
+  m = block_reduce(m, true);
+  const float T = temperature ? temperature[row] : 1.0f;
+  const bool greedy = !(T > 0.0f) || isinf(T);
+  if (greedy || m == -INFINITY) {
+    if (threadIdx.x == 0) out_lse[row] = m;
+    return;
+  }
+  float s = 0.0f;
+  for (int i = threadIdx.x; i < n_tiles; i += kLseThreads) s += expf(t[i] - m);
+  s = block_reduce(s, false);
+  if (threadIdx.x == 0) out_lse[row] = m + logf(s);
+}
+
+__device__ __forceinline__ uint32_t merge_word(const PhiloxSchedule& ks, uint64_t offset, int b,
+                                               uint32_t k) {
+  const uint4 r = philox4x32_10(make_uint4(k >> 2, static_cast<uint32_t>(b) | 0x80000000u,
+                                           static_cast<uint32_t>(offset),
+                                           static_cast<uint32_t>(offset >> 32)),
+                                ks);
+  return select_word(r, k & 3u);
+}
+
+// One thread per row.
+__global__ void __launch_bounds__(kMergeThreads)
+    group_merge_kernel(const int64_t* __restrict__ z, const float* __restrict__ m,
+                       const float* __restrict__ L, int32_t P, int32_t B, int mode,
+                       const uint64_t* __restrict__ seeds, uint64_t seed, uint64_t offset,
+                       int64_t* __restrict__ out_idx, float* __restrict__ out_L) {
+  const int b = blockIdx.x * kMergeThreads + threadIdx.x;
+  if (b >= B) return;
+  const PhiloxSchedule ks(seeds ? seeds[b] : seed);
+  float best = -INFINITY;
+  int64_t pick = -1;
+  float lmax = -INFINITY;
+  for (int k = 0; k < P; ++k) {
+    const int64_t i = int64_t(k) * B + b;
+    const int64_t zk = z[i];
+    float key;
+    bool valid = zk >= 0;
+    if (mode == FS_MERGE_EXACT) {
+      key = m[i];
+    } else {
+      const float Lk = L[i];
+      valid = valid && Lk > -INFINITY;
+      key = Lk + gumbel_from_word(merge_word(ks, offset, b, uint32_t(k)));
+    }
+    if (valid && key > best) {
+      best = key;
+      pick = zk;
+    }
+    if (L != nullptr) lmax = fmaxf(lmax, L[i]);
+  }
+  out_idx[b] = pick;
+  if (out_L != nullptr) {
+    float r = lmax;
+    if (lmax > -INFINITY) {
+      float s = 0.0f;
+      for (int k = 0; k < P; ++k) s += expf(L[int64_t(k) * B + b] - lmax);
+      r = lmax + logf(s);
+    }
+    out_L[b] = r;
+  }
+}
+
+__global__ void __launch_bounds__(kMergeThreads)
+    online_merge_kernel(int64_t* __restrict__ state_z, float* __restrict__ state_L,
+                        const int64_t* __restrict__ new_z, const float* __restrict__ new_L,
+                        int32_t B, uint64_t step, const uint64_t* __restrict__ seeds,
+                        uint64_t seed, uint64_t offset) {
+  const int b = blockIdx.x * kMergeThreads + threadIdx.x;
+  if (b >= B) return;
+  const int64_t nz = new_z[b];
+  const float nL = new_L[b];
+  if (nz < 0 || !(nL > -INFINITY)) return;
+  const float sL = state_L[b];
+  if (state_z[b] < 0 || !(sL > -INFINITY)) {  // empty state: take the group
+    state_z[b] = nz;
+    state_L[b] = nL;
+    return;
+  }
+  const float hi = fmaxf(sL, nL), lo = fminf(sL, nL);
+  const float Lp = hi + log1pf(expf(lo - hi));  // logaddexp
+  const PhiloxSchedule ks(seeds ? seeds[b] : seed);
+  const float u = uniform_from_word(merge_word(ks, offset, b, uint32_t(step)));
+  if (u < expf(nL - Lp)) state_z[b] = nz;
+  state_L[b] = Lp;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+fs_status launch_row_lse(const float* tile_lse, const float* temperature, int64_t B,
+                         int64_t n_tiles, float* out_lse, cudaStream_t stream) {
+  row_lse_kernel<<<unsigned(B), kLseThreads, 0, stream>>>(tile_lse, temperature,
+                                                          int32_t(n_tiles), out_lse);
+  if (cudaGetLastError() != cudaSuccess) return FS_ERR_CUDA;
+  return FS_OK;
+}
+
+}  // namespace fs
+
+extern "C" fs_status fs_group_merge(const int64_t* z, const float* m, const float* L, int64_t P,
+                                    int64_t B, int mode, const uint64_t* seeds, uint64_t seed,
+                                    uint64_t offset, int64_t* out_idx, float* out_L,
+                                    void* stream) {
+  using fs::aligned;
+  if (!z || !out_idx || P < 1 || B < 1 || B > 65535 || P > (int64_t(1) << 24))
+    return FS_ERR_INVALID_ARG;
+  if (mode == FS_MERGE_EXACT ? !m : mode == FS_MERGE_GROUP_GUMBEL ? !L : true)
+    return FS_ERR_INVALID_ARG;
+  if (out_L && !L) return FS_ERR_INVALID_ARG;
+  if (!aligned(z, 8) || !aligned(out_idx, 8) || (m && !aligned(m, 4)) || (L && !aligned(L, 4)) ||
+      (out_L && !aligned(out_L, 4)) || (seeds && !aligned(seeds, 8)))
+    return FS_ERR_INVALID_ARG;
+  const int blocks = int((B + fs::kMergeThreads - 1) / fs::kMergeThreads);
+  fs::group_merge_kernel<<<blocks, fs::kMergeThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      z, m, L, int32_t(P), int32_t(B), mode, seeds, seed, offset, out_idx, out_L);
+  return cudaGetLastError() == cudaSuccess ? FS_OK : FS_ERR_CUDA;
+}
+
+extern "C" fs_status fs_online_merge(int64_t* state_z, float* state_L, const int64_t* new_z,
+                                     const float* new_L, int64_t B, uint64_t step,
+                                     const uint64_t* seeds, uint64_t seed, uint64_t offset,
+                                     void* stream) {
+  using fs::aligned;
+  if (!state_z || !state_L || !new_z || !new_L || B < 1 || B > 65535 ||
+      step > uint64_t(0xFFFFFFFFu))
+    return FS_ERR_INVALID_ARG;
+  if (!aligned(state_z, 8) || !aligned(new_z, 8) || !aligned(state_L, 4) ||
+      !aligned(new_L, 4) || (seeds && !aligned(seeds, 8)))
+    return FS_ERR_INVALID_ARG;
+  const int blocks = int((B + fs::kMergeThreads - 1) / fs::kMergeThreads);
+  fs::online_merge_kernel<<<blocks, fs::kMergeThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      state_z, state_L, new_z, new_L, int32_t(B), step, seeds, seed, offset);
+  return cudaGetLastError() == cudaSuccess ? FS_OK : FS_ERR_CUDA;
+}

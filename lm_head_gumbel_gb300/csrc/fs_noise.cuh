@@ -80,9 +80,13 @@ constexpr float kLog2Ln2 = -0.5287663729448977f;  // log2(ln 2)
 //    |log2 u| >= 0.046;
 //  - q = log2 E only needs absolute accuracy.
 // The resulting g differs from the exact fp64 -log(-log u) by a few 1e-6.
-__device__ __forceinline__ float gumbel_log2_from_word(uint32_t w) {
+__device__ __forceinline__ float uniform_from_word(uint32_t w) {
   const float f = __uint_as_float(0x3F800000u | (w & 0x7FFFFFu));  // 1 + k 2^-23
-  const float u = f - 0x1.fffffep-1f;                               // k 2^-23 + 2^-24
+  return f - 0x1.fffffep-1f;                                        // k 2^-23 + 2^-24
+}
+
+__device__ __forceinline__ float gumbel_log2_from_word(uint32_t w) {
+  const float u = uniform_from_word(w);
   const float x = 1.0f - u;
   float ser = fmaf(x, 0.2f * kLog2e, 0.25f * kLog2e);
   ser = fmaf(x, ser, kLog2e / 3.0f);

@@ -76,6 +76,8 @@ struct Stage1Params {
   int32_t* tile_idx;
   float* tile_lse;
   int64_t* out_idx;            // sampled ids, or null (per-tile outputs only)
+  float* out_max;              // optional: the row's largest noisy score
+  int32_t vocab_offset;        // global id of W's first row (a multiple of 4)
   unsigned long long* row_keys;  // [B] packed (score, id) maxima, zero between calls
   uint32_t* ticket;            // CTAs finished so far, wraps back to zero
   uint64_t wait_limit_ns;
@@ -125,6 +127,12 @@ __device__ __forceinline__ unsigned long long pack_key(float m, int32_t idx) {
 
 __device__ __forceinline__ int64_t unpack_idx(unsigned long long key) {
   return key == 0ull ? int64_t(-1) : int64_t(0xFFFFFFFFu - static_cast<uint32_t>(key));
+}
+
+__device__ __forceinline__ float unpack_score(unsigned long long key) {
+  if (key == 0ull) return -INFINITY;
+  const uint32_t b = static_cast<uint32_t>(key >> 32);
+  return __uint_as_float((b & 0x80000000u) ? (b & 0x7FFFFFFFu) : ~b);
 }
 
 // One 32-column chunk of a sampling row, in base-2 units: s2 = l * (log2 e / T)
@@ -209,13 +217,13 @@ __device__ __forceinline__ void epilogue_tile(const Stage1Params& p, uint32_t ta
       else
         greedy_chunk<true>(r, allow, best, best_j);
     } else {
-      const uint32_t ctr0 = static_cast<uint32_t>(v0 >> 2);
+      const uint32_t ctr0 = static_cast<uint32_t>((p.vocab_offset + v0) >> 2);
       if (allow == 0xFFFFFFFFu)
         sample_chunk<false>(r, allow, scale2, ctr0, ctr_row, ctr_lo, ctr_hi, ks, best, best_j);
       else
         sample_chunk<true>(r, allow, scale2, ctr0, ctr_row, ctr_lo, ctr_hi, ks, best, best_j);
     }
-    if (best_j >= 0) best_idx = v0 + best_j;
+    if (best_j >= 0) best_idx = p.vocab_offset + v0 + best_j;
     if (kWantLse && !greedy) {
       float cm = -INFINITY;
 #pragma unroll
@@ -264,8 +272,11 @@ __device__ __forceinline__ void finish_rows(const Stage1Params& p) {
   __syncthreads();
   if (s_is_last) {
     __threadfence();
-    for (int r = threadIdx.x; r < p.B; r += blockDim.x)
-      p.out_idx[r] = unpack_idx(atomicExch(p.row_keys + r, 0ull));
+    for (int r = threadIdx.x; r < p.B; r += blockDim.x) {
+      const unsigned long long key = atomicExch(p.row_keys + r, 0ull);
+      p.out_idx[r] = unpack_idx(key);
+      if (p.out_max != nullptr) p.out_max[r] = unpack_score(key);
+    }
   }
 }
 
@@ -344,7 +355,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // working at the same moment read different H lines.  The start
         // depends on the vocabulary block only, so a row's sums (and its
         // sample) do not depend on the batch size.
-        const int k_start = int((uint32_t(vt) * 5u) % uint32_t(p.n_kb));
+        const int k_start =
+            int((uint32_t(vt + (p.vocab_offset >> 8)) * 5u) % uint32_t(p.n_kb));
         for (int kk = 0; kk < p.n_kb; ++kk) {
           const int kb = kk + k_start < p.n_kb ? kk + k_start : kk + k_start - p.n_kb;
           if (!waiter.wait(&empty_bar[stage], phase ^ 1u)) {
@@ -546,7 +558,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int u = pair_id; ok && u < n_units; u += n_pairs) {
         const int vt = u / n_mp, mp = u % n_mp;
-        const int k_start = int((uint32_t(vt) * 5u) % uint32_t(p.n_kb));
+        const int k_start =
+            int((uint32_t(vt + (p.vocab_offset >> 8)) * 5u) % uint32_t(p.n_kb));
         // Rows past the end are read from the last valid row instead (their
         // accumulator rows / columns are never used), so no box lies wholly
         // outside its tensor.
@@ -872,6 +885,12 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 using namespace fs;
 
+// Defined in fs_merge.cu: the per-row log-sum-exp over the tile log-masses.
+namespace fs {
+fs_status launch_row_lse(const float* tile_lse, const float* temperature, int64_t B,
+                         int64_t n_tiles, float* out_lse, cudaStream_t stream);
+}
+
 extern "C" int64_t fs_num_tiles(int64_t V) { return V <= 0 ? 0 : (V + kTileV - 1) / kTileV; }
 
 // Workspace layout: [0, 4) the CTA ticket, [256, 256 + 8B) the per-row keys.
@@ -914,6 +933,11 @@ extern "C" fs_status fs_sample(const fs_sample_args* a, void* stream_ptr) {
     return FS_ERR_INVALID_ARG;
   if (a->out_tile_lse && (!aligned(a->out_tile_lse, 4) || !a->out_tile_max))
     return FS_ERR_INVALID_ARG;
+  if (a->vocab_offset < 0 || a->vocab_offset % 4 != 0 ||
+      a->vocab_offset + V > int64_t(0x7FFFFFFF))
+    return FS_ERR_INVALID_ARG;
+  if (a->out_max && (!a->out_idx || !aligned(a->out_max, 4))) return FS_ERR_INVALID_ARG;
+  if (a->out_lse && (!a->out_tile_lse || !aligned(a->out_lse, 4))) return FS_ERR_INVALID_ARG;
 
   const int64_t n_tiles = fs_num_tiles(V);
   if (a->out_idx != nullptr) {
@@ -964,6 +988,8 @@ extern "C" fs_status fs_sample(const fs_sample_args* a, void* stream_ptr) {
   p.tile_idx = a->out_tile_idx;
   p.tile_lse = a->out_tile_lse;
   p.out_idx = a->out_idx;
+  p.out_max = a->out_max;
+  p.vocab_offset = int32_t(a->vocab_offset);
   p.ticket = a->out_idx ? static_cast<uint32_t*>(a->workspace) : nullptr;
   p.row_keys = a->out_idx ? reinterpret_cast<unsigned long long*>(
                                 static_cast<uint8_t*>(a->workspace) + kKeysOffset)
@@ -985,7 +1011,8 @@ extern "C" fs_status fs_sample(const fs_sample_args* a, void* stream_ptr) {
   else
     lst = lse ? launch_stage1<true, 1>(tmap_h, tmap_w, p, mc, stream)
               : launch_stage1<false, 1>(tmap_h, tmap_w, p, mc, stream);
-  return lst;
+  if (lst != FS_OK || a->out_lse == nullptr) return lst;
+  return launch_row_lse(a->out_tile_lse, a->temperature, B, n_tiles, a->out_lse, stream);
 }
 
 // ---- allocation-free variant ---------------------------------------------

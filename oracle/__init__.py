@@ -52,6 +52,8 @@ class Oracle:
         L.fso_noise_word.restype = _u32
         L.fso_noise.argtypes = [_u64, _u64, _i64, _i64]
         L.fso_noise.restype = ctypes.c_double
+        L.fso_merge_uniform.argtypes = [_u64, _u64, _i64, _i64]
+        L.fso_merge_uniform.restype = ctypes.c_double
         L.fso_noise_grid.argtypes = [_ptr, _u64, _u64, _i64, _i64, _i64, _i64, _ptr]
         L.fso_noise_grid.restype = None
         L.fso_logits.argtypes = [_ptr, _ptr, _i64, _i64, _i64, _i64, _i64, _ptr]
@@ -85,6 +87,13 @@ class Oracle:
 
     def noise(self, seed: int, offset: int, b: int, v: int) -> float:
         return self.lib.fso_noise(seed, offset, b, v)
+
+    def merge_uniform(self, seed: int, offset: int, b: int, k: int) -> float:
+        """The uniform a merge draws for row b and partition / step k."""
+        return self.lib.fso_merge_uniform(int(seed) & (2**64 - 1), int(offset) & (2**64 - 1), b, k)
+
+    def merge_uniforms(self, seed: int, offset: int, b: int, n: int):
+        return np.array([self.merge_uniform(seed, offset, b, k) for k in range(n)])
 
     def noise_grid(self, b0, nb, v0, nv, seed=0, offset=0, seeds=None):
         out = np.empty((nb, nv), dtype=np.float64)

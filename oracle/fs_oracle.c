@@ -98,6 +98,23 @@ double fso_noise(uint64_t seed, uint64_t offset, int64_t b, int64_t v) {
   return fso_gumbel(fso_uniform(fso_noise_word(seed, offset, b, v)));
 }
 
+/* The uniform that merges draw for row b and partition (or online step) k:
+ * Philox4x32-10 with the row's key and counter (k >> 2, b | 2^31, offset low,
+ * offset high), word k & 3 -- a counter domain the sampling noise never uses
+ * (its second counter word is the row, below 2^31), so the choice among
+ * partitions is independent of the partitions' own samples. */
+double fso_merge_uniform(uint64_t seed, uint64_t offset, int64_t b, int64_t k) {
+  uint32_t counter[4], key[2], out[4];
+  counter[0] = (uint32_t)((uint64_t)k >> 2);
+  counter[1] = (uint32_t)b | 0x80000000u;
+  counter[2] = (uint32_t)(offset & 0xffffffffu);
+  counter[3] = (uint32_t)(offset >> 32);
+  key[0] = (uint32_t)(seed & 0xffffffffu);
+  key[1] = (uint32_t)(seed >> 32);
+  fso_philox4x32_10(counter, key, out);
+  return fso_uniform(out[(uint64_t)k & 3u]);
+}
+
 /* Noise for the window rows [b0, b0+nb) x vocab [v0, v0+nv), row-major.
  * seeds (optional) gives one seed per absolute row index. */
 void fso_noise_grid(const uint64_t *seeds, uint64_t seed, uint64_t offset,

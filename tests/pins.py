@@ -330,6 +330,24 @@ def pin_max_stability(o):
         assert ks.pvalue > P_MIN, (t, ks)
 
 
+def pin_merge_uniform(o):
+    """The merge uniforms: Philox on their own counter domain (second word
+    row | 2^31), uniform on (0,1), uncorrelated with the sampling noise of the
+    same (row, index), and exact in fp32."""
+    seed, off = 4242, (3 << 32) + 17
+    for b, k in ((0, 0), (5, 3), (7, 9), (1000, 4)):
+        w = o.philox([k >> 2, b | 0x80000000, off & 0xFFFFFFFF, off >> 32],
+                     [seed & 0xFFFFFFFF, seed >> 32])[k & 3]
+        assert o.merge_uniform(seed, off, b, k) == o.uniform(int(w))
+    us = np.array([[o.merge_uniform(seed, off, b, k) for k in range(512)] for b in range(16)])
+    assert np.all((us > 0) & (us < 1))
+    ks = scipy.stats.kstest(us.ravel(), "uniform")
+    assert ks.pvalue > P_MIN, ks
+    words = np.array([[o.noise_word(seed, off, b, k) for k in range(512)] for b in range(16)])
+    samp = (words & 0x7FFFFF).astype(np.float64)
+    assert abs(np.corrcoef(us.ravel(), samp.ravel())[0, 1]) < 0.02
+
+
 def pin_group_merges(o):
     """Group-Gumbel-Max and the online binary merge over 4 vocabulary groups,
     fed the groups' own samples and log-masses, follow softmax(l / T)."""
@@ -382,4 +400,5 @@ ALL_PINS = [
     pin_masked_distribution,
     pin_max_stability,
     pin_group_merges,
+    pin_merge_uniform,
 ]

@@ -31,7 +31,8 @@ def declared_functions():
 def test_header_declares_entry_points():
     names = declared_functions()
     for want in ("fs_sample", "fs_workspace_size", "fs_num_tiles", "fs_status_string",
-                 "fs_gumbel_noise", "fs_last_device_error"):
+                 "fs_gumbel_noise", "fs_last_device_error", "fs_group_merge", "fs_online_merge",
+                 "fs_sample_noalloc", "fs_wait_timeout_selftest"):
         assert want in names
 
 
@@ -88,6 +89,8 @@ def _args(**kw):
     (dict(out_tile_idx=None), 1), (dict(out_tile_max=None), 1),
     (dict(vocab_mask=0x60000, mask_ld=127), 1),
     (dict(out_tile_lse=0x80000, out_tile_max=None, out_tile_idx=None), 1),
+    (dict(vocab_offset=-4), 1), (dict(vocab_offset=6), 1), (dict(vocab_offset=2**31 - 4096), 1),
+    (dict(out_max=0x90000, out_idx=None), 1), (dict(out_lse=0x90000), 1),
     (dict(), 5),                                   # sampling without a workspace
     (dict(out_tile_max=None, out_tile_idx=None), 5),
     (dict(out_tile_max=None, out_tile_idx=None, workspace=0x70000, workspace_bytes=511), 5),
@@ -119,3 +122,21 @@ def test_package_fails_loudly_without_library(tmp_path):
             bnd.load_library(str(tmp_path / "missing.so"))
     finally:
         bnd._lib = saved
+
+
+def test_merge_bad_arguments(lib):
+    p = ctypes.c_void_p
+    z, m, L, o = p(0x10000), p(0x20000), p(0x30000), p(0x40000)
+    gm = lib.fs_group_merge
+    assert gm(None, m, L, 2, 4, 0, None, 0, 0, o, None, None) == 1      # no z
+    assert gm(z, m, L, 0, 4, 0, None, 0, 0, o, None, None) == 1         # P < 1
+    assert gm(z, m, L, 2, 0, 0, None, 0, 0, o, None, None) == 1         # B < 1
+    assert gm(z, None, L, 2, 4, 0, None, 0, 0, o, None, None) == 1      # exact needs m
+    assert gm(z, m, None, 2, 4, 1, None, 0, 0, o, None, None) == 1      # group needs L
+    assert gm(z, m, L, 2, 4, 7, None, 0, 0, o, None, None) == 1         # unknown mode
+    assert gm(z, m, None, 2, 4, 0, None, 0, 0, o, p(0x50000), None) == 1  # out_L needs L
+    assert gm(p(0x10004), m, L, 2, 4, 0, None, 0, 0, o, None, None) == 1  # misaligned z
+    om = lib.fs_online_merge
+    assert om(None, L, z, L, 4, 0, None, 0, 0, None) == 1
+    assert om(z, L, z, L, 0, 0, None, 0, 0, None) == 1
+    assert om(z, L, z, L, 4, 2**33, None, 0, 0, None) == 1

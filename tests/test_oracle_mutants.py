@@ -53,6 +53,8 @@ MUTANTS = [
     ("greedy-adds-noise", "lp[v] = l[v];\n        s[v] = l[v];",
      "lp[v] = l[v];\n        s[v] = l[v] + fso_noise(sd, offset, b, v);", 0),
     ("tile-boundary-short", "hi = (lo + tile < V) ? lo + tile : V;", "hi = (lo + tile < V) ? lo + tile - 1 : V;", 0),
+    ("merge-domain-not-separated", "counter[1] = (uint32_t)b | 0x80000000u;",
+     "counter[1] = (uint32_t)b;", 0),
     ("per-row-seed-ignored", "uint64_t sd = seeds ? seeds[b] : seed;\n    for", "uint64_t sd = seed;\n    for", 0),
 ]
 
