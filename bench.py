@@ -296,6 +296,25 @@ def run_ours(args):
                           "achieved": rf["achieved"], "unit": rf["unit"], "frac": rf["frac"],
                           "window": (ts0, time.time())})
             del inp2, o2, ws2
+    # The K-draws-without-replacement mode on the same batch (an extension of
+    # the headline path; reported beside it, not in it).
+    extensions = {}
+    if world == 1 and not args.no_sweep:
+        for K in (4, 16):
+            tk_out = torch.empty((B, K), dtype=torch.int64, device=dev)
+            tk_ws = torch.empty(fs.fs_topk_workspace_size(B, V, K), dtype=torch.uint8, device=dev)
+
+            def ctk(k, K=K, tk_out=tk_out, tk_ws=tk_ws):
+                fs.fs_sample_topk(inp["H"], inp["W"], K, temperature=inp["temperature"],
+                                  seeds=inp["seeds"], offset=k, out_topk_idx=tk_out,
+                                  workspace=tk_ws, stream=stream)
+
+            for k in range(3):
+                ctk(k)
+            us_tk = time_calls(ctk, args.sweep_steps, stream) * 1000.0 / args.sweep_steps
+            extensions[f"topk{K}_us_per_call"] = round(us_tk, 2)
+            del tk_out, tk_ws
+
     # End to end through the C ABI: each step's inputs (H, temperatures, seeds)
     # go host -> device in one copy from one pinned buffer, fs_sample runs from
     # an argument block built once (only the offset changes), and the sampled
@@ -386,6 +405,7 @@ def run_ours(args):
         "gpu_launches": args.steps,
         "clocks": ClockSampler.summarize(clock_rows, t_wall0, t_wall1),
         "sweep": sweep,
+        "extensions": extensions,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inp, B, args.cpu_seconds)

@@ -169,6 +169,32 @@ fs_status fs_sample(const fs_sample_args *args, void *stream);
  */
 fs_status fs_sample_noalloc(const fs_sample_args *args, void *stream);
 
+/* Largest K of fs_sample_topk. */
+#define FS_TOPK_MAX 16
+
+/* Bytes of workspace fs_sample_topk needs: B * ceil(V/128) * C * 8 with
+ * C = 4 for K <= 4 and 16 otherwise, rounded up to 256 (0 for bad sizes).
+ * It needs no initialisation. */
+size_t fs_topk_workspace_size(int64_t B, int64_t V, int64_t K);
+
+/*
+ * K distinct samples per row, without replacement, in draw order: the ids of
+ * the K largest noisy scores s[b, v] (ties to the lower id).  By the Gumbel-
+ * top-k property of the Gumbel-max trick this is a draw of K tokens without
+ * replacement from softmax(l'[b, :]) (the aitrends.kr write-up notes the design
+ * extends to top-k); out_topk_idx[b, 0] is the id fs_sample returns for the
+ * same inputs.  Greedy rows give the K largest logits.  The stage-1 kernel
+ * keeps the best 4 (K <= 4) or 16 (K <= 16) scores of every (row, 128-id tile)
+ * in the workspace (args->workspace, fs_topk_workspace_size bytes, 256-byte
+ * aligned, no initialisation needed) and a second kernel merges them per row.
+ * Uses args' inputs (H, W, temperature, mask, seeds, offset, vocab_offset);
+ * args' outputs (out_idx, out_tile_*, out_max, out_lse) must be NULL.
+ * out_topk_idx: int64 [B, K] (-1 past the row's unmasked count);
+ * out_topk_score: fp32 [B, K] or NULL (the scores, -inf past the count).
+ */
+fs_status fs_sample_topk(const fs_sample_args *args, int64_t K, int64_t *out_topk_idx,
+                         float *out_topk_score, void *stream);
+
 /* Merge rules of fs_group_merge. */
 #define FS_MERGE_EXACT 0        /* argmax_k m_k: the sample of the union       */
 #define FS_MERGE_GROUP_GUMBEL 1 /* argmax_k L_k + G_k with fresh Gumbel noise  */

@@ -21,6 +21,7 @@ FS_ERR_UNSUPPORTED = 2
 FS_ERR_CUDA = 3
 FS_ERR_DEVICE_TIMEOUT = 4
 FS_ERR_WORKSPACE = 5
+FS_TOPK_MAX = 16
 FS_MERGE_EXACT = 0
 FS_MERGE_GROUP_GUMBEL = 1
 
@@ -72,6 +73,10 @@ def load_library(path: str = LIB_PATH):
     lib.fs_gumbel_noise.argtypes = [_c_ptr, _c_u64, _c_u64, _c_i64, _c_i64, _c_i64, _c_i64,
                                     _c_ptr, _c_ptr]
     lib.fs_gumbel_noise.restype = ctypes.c_int
+    lib.fs_topk_workspace_size.argtypes = [_c_i64, _c_i64, _c_i64]
+    lib.fs_topk_workspace_size.restype = ctypes.c_size_t
+    lib.fs_sample_topk.argtypes = [ctypes.POINTER(FsSampleArgs), _c_i64, _c_ptr, _c_ptr, _c_ptr]
+    lib.fs_sample_topk.restype = ctypes.c_int
     lib.fs_group_merge.argtypes = [_c_ptr, _c_ptr, _c_ptr, _c_i64, _c_i64, ctypes.c_int, _c_ptr,
                                    _c_u64, _c_u64, _c_ptr, _c_ptr, _c_ptr]
     lib.fs_group_merge.restype = ctypes.c_int
@@ -190,6 +195,42 @@ def fs_sample(H, W, *, temperature=None, vocab_mask=None, seeds=None, seed=0, of
     if st != FS_OK:
         raise FsError(st, "fs_sample")
     return out_idx
+
+
+def fs_topk_workspace_size(B: int, V: int, K: int) -> int:
+    return int(load_library().fs_topk_workspace_size(int(B), int(V), int(K)))
+
+
+def fs_sample_topk(H, W, K, *, temperature=None, vocab_mask=None, seeds=None, seed=0, offset=0,
+                   vocab_offset=0, out_topk_idx=None, out_topk_score=None, workspace=None,
+                   stream=None):
+    """K draws without replacement per row (the K largest noisy scores, in
+    draw order).  Returns out_topk_idx (int64 [B, K]); fills out_topk_score
+    (fp32 [B, K]) when given."""
+    lib = load_library()
+    _check_2d("H", H, torch.bfloat16)
+    _check_2d("W", W, torch.bfloat16)
+    B, d = H.shape
+    V = W.shape[0]
+    dev = H.device
+    if out_topk_idx is None:
+        out_topk_idx = torch.empty((B, K), dtype=torch.int64, device=dev)
+    if workspace is None:
+        workspace = torch.empty(max(1, fs_topk_workspace_size(B, V, K)), dtype=torch.uint8,
+                                device=dev)
+    mask_ld = 0 if vocab_mask is None else vocab_mask.stride(0)
+    args = FsSampleArgs(
+        H=_ptr(H), W=_ptr(W), temperature=_ptr(temperature), vocab_mask=_ptr(vocab_mask),
+        mask_ld=mask_ld, seeds=_ptr(seeds), seed=int(seed) & (2**64 - 1),
+        offset=int(offset) & (2**64 - 1), B=B, d=d, V=V, ldh=H.stride(0), ldw=W.stride(0),
+        workspace=_ptr(workspace), workspace_bytes=workspace.numel() * workspace.element_size(),
+        vocab_offset=int(vocab_offset))
+    with torch.cuda.device(dev):
+        st = lib.fs_sample_topk(ctypes.byref(args), int(K), _ptr(out_topk_idx),
+                                _ptr(out_topk_score), _stream_handle(stream, dev))
+    if st != FS_OK:
+        raise FsError(st, "fs_sample_topk")
+    return out_topk_idx
 
 
 def fs_group_merge(z, *, m=None, L=None, mode=FS_MERGE_EXACT, seeds=None, seed=0, offset=0,

@@ -11,7 +11,8 @@
 //                       exact (argmax_k m_k) or Group-Gumbel-Max
 //                       (argmax_k L_k + G_k, fresh Gumbel noise);
 //   online_merge_kernel the O(1)-state binary merge rule with a Bernoulli
-//                       switch, one group at a time.
+//                       switch, one group at a time;
+//   topk_reduce_kernel  each row's K best of its per-tile top-K candidates.
 // The merges' own randomness uses Philox on a counter domain the sampling noise
 // never uses (second counter word = row | 2^31), keyed by the row's seed.
 #include <cuda_runtime.h>
@@ -143,7 +144,103 @@ __global__ void __launch_bounds__(kMergeThreads)
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// The order of (score, id) candidates: higher score first, then lower id; an
+// id of -1 (no candidate) comes after everything.
+__device__ __forceinline__ bool precedes(float as, int32_t ai, float bs, int32_t bi) {
+  return ai >= 0 && (bi < 0 || as > bs || (as == bs && ai < bi));
+}
+
+constexpr int kTopkThreads = 128;
+constexpr int kTopkCap = FS_TOPK_MAX;
+
+// Each row's K best of its per-tile candidates (Gumbel-top-k: K draws without
+// replacement, in draw order).  One block per row: every thread keeps the
+// kTopkCap best of its share, then K rounds pick the best remaining head.
+__global__ void __launch_bounds__(kTopkThreads)
+    topk_reduce_kernel(const float* __restrict__ cand_score,
+                       const int32_t* __restrict__ cand_idx, int64_t n_cand, int32_t K,
+                       int64_t* __restrict__ out_idx, float* __restrict__ out_score) {
+  const int row = blockIdx.x;
+  const float* cs = cand_score + int64_t(row) * n_cand;
+  const int32_t* ci = cand_idx + int64_t(row) * n_cand;
+  float ls[kTopkCap];
+  int32_t li[kTopkCap];
+#pragma unroll
+  for (int q = 0; q < kTopkCap; ++q) {
+    ls[q] = -INFINITY;
+    li[q] = -1;
+  }
+  for (int64_t c = threadIdx.x; c < n_cand; c += kTopkThreads) {
+    const float sc = cs[c];
+    const int32_t ic = ci[c];
+    if (!precedes(sc, ic, ls[kTopkCap - 1], li[kTopkCap - 1])) continue;
+    ls[kTopkCap - 1] = sc;
+    li[kTopkCap - 1] = ic;
+#pragma unroll
+    for (int q = kTopkCap - 1; q > 0; --q) {
+      const bool up = precedes(ls[q], li[q], ls[q - 1], li[q - 1]);
+      const float a = ls[q], b = ls[q - 1];
+      const int32_t ia = li[q], ib = li[q - 1];
+      ls[q - 1] = up ? a : b;
+      ls[q] = up ? b : a;
+      li[q - 1] = up ? ia : ib;
+      li[q] = up ? ib : ia;
+    }
+  }
+  __shared__ float ws[kTopkThreads / 32];
+  __shared__ int32_t wi[kTopkThreads / 32];
+  __shared__ float win_s;
+  __shared__ int32_t win_i;
+  for (int j = 0; j < K; ++j) {
+    float bs = ls[0];
+    int32_t bi = li[0];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float os = __shfl_xor_sync(0xFFFFFFFFu, bs, off);
+      const int32_t oi = __shfl_xor_sync(0xFFFFFFFFu, bi, off);
+      if (precedes(os, oi, bs, bi)) {
+        bs = os;
+        bi = oi;
+      }
+    }
+    if ((threadIdx.x & 31) == 0) {
+      ws[threadIdx.x >> 5] = bs;
+      wi[threadIdx.x >> 5] = bi;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int w = 1; w < kTopkThreads / 32; ++w)
+        if (precedes(ws[w], wi[w], bs, bi)) {
+          bs = ws[w];
+          bi = wi[w];
+        }
+      win_s = bs;
+      win_i = bi;
+      out_idx[int64_t(row) * K + j] = bi;
+      if (out_score != nullptr) out_score[int64_t(row) * K + j] = bi >= 0 ? bs : -INFINITY;
+    }
+    __syncthreads();
+    if (li[0] >= 0 && li[0] == win_i) {  // this thread held the winner: pop it
+#pragma unroll
+      for (int q = 0; q < kTopkCap - 1; ++q) {
+        ls[q] = ls[q + 1];
+        li[q] = li[q + 1];
+      }
+      ls[kTopkCap - 1] = -INFINITY;
+      li[kTopkCap - 1] = -1;
+    }
+  }
+}
+
 }  // namespace
+
+fs_status launch_topk_reduce(const float* cand_score, const int32_t* cand_idx, int64_t B,
+                             int64_t n_cand, int64_t K, int64_t* out_idx, float* out_score,
+                             cudaStream_t stream) {
+  topk_reduce_kernel<<<unsigned(B), kTopkThreads, 0, stream>>>(cand_score, cand_idx, n_cand,
+                                                               int32_t(K), out_idx, out_score);
+  return cudaGetLastError() == cudaSuccess ? FS_OK : FS_ERR_CUDA;
+}
 
 fs_status launch_row_lse(const float* tile_lse, const float* temperature, int64_t B,
                          int64_t n_tiles, float* out_lse, cudaStream_t stream) {

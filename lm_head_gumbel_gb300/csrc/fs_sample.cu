@@ -64,8 +64,6 @@ struct Stage1Params {
   int32_t B, V, d;
   int32_t n_tiles;   // ceil(V / 128)
   int32_t n_mt;      // ceil(B / 128)
-  int32_t n_mgroups; // ceil(n_mt / cluster size)
-  int32_t n_cunits;  // ceil(V / 256) * n_mgroups: units of work per cluster
   int32_t n_kb;      // ceil(d / 64)
   const float* temperature;
   const uint32_t* mask;
@@ -80,6 +78,8 @@ struct Stage1Params {
   int32_t vocab_offset;        // global id of W's first row (a multiple of 4)
   unsigned long long* row_keys;  // [B] packed (score, id) maxima, zero between calls
   uint32_t* ticket;            // CTAs finished so far, wraps back to zero
+  float* topk_score;           // top-K modes: [B, n_tiles, cap] best scores per tile
+  int32_t* topk_idx;           //              [B, n_tiles, cap] their global ids
   uint64_t wait_limit_ns;
   uint32_t h_box_rows;  // rows of the H box: min(128, B rounded up to 8)
 };
@@ -257,6 +257,98 @@ __device__ __forceinline__ void epilogue_tile(const Stage1Params& p, uint32_t ta
   }
 }
 
+// Insert (s, id) into a list sorted by decreasing score whose last entry it
+// beats.  Equal scores keep their order, so with ids visited in increasing
+// order the lower id stays first (the tie rule).
+template <int KC>
+__device__ __forceinline__ void topk_insert(float (&ts)[KC], int32_t (&ti)[KC], float s,
+                                            int32_t id) {
+  ts[KC - 1] = s;
+  ti[KC - 1] = id;
+#pragma unroll
+  for (int q = KC - 1; q > 0; --q) {
+    const bool up = ts[q] > ts[q - 1];
+    const float a = ts[q], b = ts[q - 1];
+    const int32_t ia = ti[q], ib = ti[q - 1];
+    ts[q - 1] = up ? a : b;
+    ts[q] = up ? b : a;
+    ti[q - 1] = up ? ia : ib;
+    ti[q] = up ? ib : ia;
+  }
+}
+
+// Top-K form of epilogue_tile: the KC largest noisy scores of the row's tile
+// and their global ids, best first (-inf / -1 past the unmasked count),
+// written to the workspace.  By the Gumbel-top-k property the K largest scores
+// of a row are K draws without replacement from softmax(l'), in draw order.
+template <int KC>
+__device__ __forceinline__ void epilogue_tile_topk(const Stage1Params& p, uint32_t taddr,
+                                                   int row, int tile) {
+  const bool valid_row = row < p.B;
+  float T = 1.0f;
+  uint64_t seed = p.seed;
+  const uint32_t* mrow = nullptr;
+  if (valid_row) {
+    if (p.temperature) T = p.temperature[row];
+    if (p.seeds) seed = p.seeds[row];
+    if (p.mask) mrow = p.mask + int64_t(row) * p.mask_ld;
+  }
+  const bool greedy = !(T > 0.0f) || isinf(T);
+  const float scale2 = greedy ? 1.0f : kLog2e / T;
+  const PhiloxSchedule ks(seed);
+  const uint32_t ctr_row = static_cast<uint32_t>(row);
+  const uint32_t ctr_lo = static_cast<uint32_t>(p.offset);
+  const uint32_t ctr_hi = static_cast<uint32_t>(p.offset >> 32);
+  float ts[KC];
+  int32_t ti[KC];
+#pragma unroll
+  for (int q = 0; q < KC; ++q) {
+    ts[q] = -INFINITY;
+    ti[q] = -1;
+  }
+  const int v_tile = tile * kTileV;
+#pragma unroll 1
+  for (int c = 0; c < kTileV / 32; ++c) {
+    uint32_t r[32];
+    ptx::tmem_ld_32x32b_x32(taddr + uint32_t(c * 32), r);
+    ptx::tmem_wait_ld();
+    if (!valid_row) continue;
+    const int v0 = v_tile + c * 32;
+    uint32_t allow = mrow ? mrow[v0 >> 5] : 0xFFFFFFFFu;
+    const int n_in = p.V - v0;
+    if (n_in < 32) allow &= (n_in <= 0) ? 0u : ((1u << n_in) - 1u);
+    const int32_t id0 = p.vocab_offset + v0;
+    if (greedy) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float l = __uint_as_float(r[j]);
+        if (((allow >> j) & 1u) && l > ts[KC - 1]) topk_insert<KC>(ts, ti, l, id0 + j);
+      }
+      continue;
+    }
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      const uint4 rnd = philox4x32_10(
+          make_uint4(static_cast<uint32_t>(id0 >> 2) + g, ctr_row, ctr_lo, ctr_hi), ks);
+      const uint32_t words[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int j = g * 4 + i;
+        const float s2 = fmaf(__uint_as_float(r[j]), scale2, -gumbel_log2_from_word(words[i]));
+        if (((allow >> j) & 1u) && s2 > ts[KC - 1]) topk_insert<KC>(ts, ti, s2, id0 + j);
+      }
+    }
+  }
+  if (!valid_row) return;
+  const int64_t o = (int64_t(row) * p.n_tiles + tile) * KC;
+#pragma unroll
+  for (int q = 0; q < KC; ++q) {
+    const float m = (greedy || ti[q] < 0) ? ts[q] : kLn2 * (ts[q] - kLog2Ln2);
+    p.topk_score[o + q] = m;
+    p.topk_idx[o + q] = ti[q];
+  }
+}
+
 // Stage 2 ("Stage 2 (Reduction)"), fused: the last CTA to finish turns the
 // per-row maxima into sampled ids and clears them for the next call.  The
 // ticket wraps to zero on the last arrival, so it too is left cleared.  Called
@@ -280,20 +372,34 @@ __device__ __forceinline__ void finish_rows(const Stage1Params& p) {
   }
 }
 
-// Work decomposition: a unit is (vocabulary block vt of 256 ids, batch block mt
-// of 128 rows).  CTAs run in clusters of kCluster along the batch dimension: the
-// CTAs of a cluster take the kCluster batch blocks of one group of one
-// vocabulary block, each loads 1/kCluster of the W slice and multicasts it to
-// the whole cluster, so W crosses L2 -> SM once per cluster instead of once per
-// CTA.  A stage is refilled only after every CTA of the cluster has consumed it
-// (the MMA commits are multicast to every CTA's "empty" barrier).
-template <bool kWantLse, int kCluster>
+// Epilogue modes (a template parameter of both stage-1 kernels).
+enum : int {
+  kModeSample = 0,  // (m_t, i_t) per tile, row maxima
+  kModeLse = 1,     // ... plus the tile log-sum-exp
+  kModeTop4 = 2,    // the 4 best (score, id) per tile, for K <= 4 draws without replacement
+  kModeTop16 = 3,   // the 16 best, for K <= 16
+};
+__host__ __device__ constexpr int topk_cap(int mode) {
+  return mode == kModeTop4 ? 4 : mode == kModeTop16 ? 16 : 1;
+}
+
+template <int kMode>
+__device__ __forceinline__ void epilogue_unit(const Stage1Params& p, uint32_t taddr, int row,
+                                              int tile) {
+  if constexpr (kMode == kModeSample || kMode == kModeLse)
+    epilogue_tile<kMode == kModeLse>(p, taddr, row, tile);
+  else
+    epilogue_tile_topk<topk_cap(kMode)>(p, taddr, row, tile);
+}
+
+// Single-CTA stage 1: a unit is (vocabulary block vt of 256 ids, batch block mt
+// of 128 rows), computed by one CTA with M = 128, N = 256 MMAs; units are
+// ordered vocabulary-major so the batch blocks of one vocabulary block run on
+// neighbouring CTAs at the same time and the second read of W hits L2.
+template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     stage1_kernel(const __grid_constant__ CUtensorMap tmap_h,
                   const __grid_constant__ CUtensorMap tmap_w, const Stage1Params p) {
-  static_assert(kCluster == 1 || kCluster == 2 || kCluster == 4, "cluster of 1, 2 or 4 CTAs");
-  constexpr uint32_t kRowsW = kBlockN / kCluster;  // W rows this CTA loads per stage
-  constexpr uint16_t kMask = uint16_t((1u << kCluster) - 1u);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -307,14 +413,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int rank = kCluster > 1 ? int(ptx::cluster_ctarank()) : 0;
-  const int cluster_id = int(blockIdx.x) / kCluster;
-  const int n_clusters = int(gridDim.x) / kCluster;
+  const int n_units = ((p.V + kBlockN - 1) / kBlockN) * p.n_mt;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       ptx::mbar_init(&full_bar[s], 1);
-      ptx::mbar_init(&empty_bar[s], kCluster);
+      ptx::mbar_init(&empty_bar[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&tfull_bar[a], 1);
@@ -335,26 +439,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
-  // Every CTA's barriers exist before any peer multicasts into them.
-  if (kCluster > 1) ptx::cluster_sync();
   const uint32_t tmem_base = *tmem_holder;
   const Waiter waiter{abort_flag, p.wait_limit_ns};
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      const uint64_t pol_w = p.n_mt > kCluster ? ptx::policy_evict_normal()
-                                               : ptx::policy_evict_first();
+      const uint64_t pol_w = p.n_mt > 1 ? ptx::policy_evict_normal() : ptx::policy_evict_first();
       const uint64_t pol_h = ptx::policy_evict_last();
       uint32_t stage = 0, phase = 0, issued = 0;
       bool ok = true;
-      for (int cu = cluster_id; ok && cu < p.n_cunits; cu += n_clusters) {
-        const int vt = cu / p.n_mgroups;
-        const int mt = (cu % p.n_mgroups) * kCluster + rank;
+      for (int unit = blockIdx.x; ok && unit < n_units; unit += gridDim.x) {
+        const int vt = unit / p.n_mt, mt = unit % p.n_mt;
         // Each vocabulary block starts its K loop at its own slice, so CTAs
         // working at the same moment read different H lines.  The start
-        // depends on the vocabulary block only, so a row's sums (and its
-        // sample) do not depend on the batch size.
+        // depends on the (global) vocabulary block only, so a row's sums (and
+        // its sample) do not depend on the batch size or on the sharding.
         const int k_start =
             int((uint32_t(vt + (p.vocab_offset >> 8)) * 5u) % uint32_t(p.n_kb));
         for (int kk = 0; kk < p.n_kb; ++kk) {
@@ -365,17 +465,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t* sa = smem + size_t(stage) * kStageBytes;
           ptx::mbar_arrive_expect_tx(&full_bar[stage], kSmemB + p.h_box_rows * 128u);
-          if (kCluster == 1) {
-            ptx::tma_load_2d(sa + kSmemA, &tmap_w, &full_bar[stage], kb * kBlockK, vt * kBlockN,
-                             pol_w);
-          } else {
-            // In the last vocabulary block a slice may start past V; it is
-            // then read from the last valid row instead (those ids are masked
-            // in the epilogue), so no box lies wholly outside the tensor.
-            const int wy = min(vt * kBlockN + rank * int(kRowsW), p.V - 1);
-            ptx::tma_load_2d_multicast(sa + kSmemA + rank * kRowsW * 128u, &tmap_w,
-                                       &full_bar[stage], kb * kBlockK, wy, kMask, pol_w);
-          }
+          ptx::tma_load_2d(sa + kSmemA, &tmap_w, &full_bar[stage], kb * kBlockK, vt * kBlockN,
+                           pol_w);
           ptx::tma_load_2d(sa, &tmap_h, &full_bar[stage], kb * kBlockK, mt * kBlockM, pol_h);
           ++issued;
           if (++stage == kStages) {
@@ -397,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
-      for (int cu = cluster_id; ok && cu < p.n_cunits; cu += n_clusters) {
+      for (int unit = blockIdx.x; ok && unit < n_units; unit += gridDim.x) {
         if (!waiter.wait(&tempty_bar[acc], acc_phase ^ 1u)) break;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * kBlockN;
@@ -415,10 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                           ptx::smem_desc_sw128(sb + k * kUmmaK * 2), kIdesc,
                           (kb | k) != 0 ? 1u : 0u);
           }
-          if (kCluster == 1)
-            ptx::mma_commit(&empty_bar[stage]);
-          else
-            ptx::mma_commit_multicast(&empty_bar[stage], kMask);
+          ptx::mma_commit(&empty_bar[stage]);
           if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
@@ -440,9 +528,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;  // the tensor-memory lane quadrant this warp may read
     const int half = e >> 2;    // which 128-column half of the unit
     uint32_t acc = 0, acc_phase = 0;
-    for (int cu = cluster_id; cu < p.n_cunits; cu += n_clusters) {
-      const int vt = cu / p.n_mgroups;
-      const int mt = (cu % p.n_mgroups) * kCluster + rank;
+    for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
+      const int vt = unit / p.n_mt, mt = unit % p.n_mt;
       int ok = 0;
       if (lane == 0) ok = waiter.wait(&tfull_bar[acc], acc_phase) ? 1 : 0;
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
@@ -453,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (row0 < p.B && tile < p.n_tiles) {
         const uint32_t taddr =
             tmem_base + (uint32_t(quad * 32) << 16) + acc * kBlockN + uint32_t(half * kTileV);
-        epilogue_tile<kWantLse>(p, taddr, row0 + lane, tile);
+        epilogue_unit<kMode>(p, taddr, row0 + lane, tile);
       }
       ptx::tc_fence_before();
       __syncwarp();
@@ -470,10 +557,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem_base, kTmemCols);
   }
-  // No CTA leaves while a peer may still multicast into it or arrive on its
-  // barriers.
-  if (kCluster > 1) ptx::cluster_sync();
-
   finish_rows(p);
 }
 
@@ -497,7 +580,7 @@ constexpr size_t kPairSmemBytes = 1024 + kPairBarOffset + 256;
 constexpr uint32_t kPairIdesc = ptx::idesc_bf16_f32(2 * kBlockM, kBlockN);
 static_assert(kPairSmemBytes <= 232448, "pair kernel shared memory");
 
-template <bool kWantLse>
+template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     stage1_pair_kernel(const __grid_constant__ CUtensorMap tmap_h,
                        const __grid_constant__ CUtensorMap tmap_w, const Stage1Params p) {
@@ -651,7 +734,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (row0 < p.B && tile < p.n_tiles) {
         const uint32_t taddr =
             tmem_base + (uint32_t(quad * 32) << 16) + acc * kBlockN + uint32_t(half * kTileV);
-        epilogue_tile<kWantLse>(p, taddr, row0 + lane, tile);
+        epilogue_unit<kMode>(p, taddr, row0 + lane, tile);
       }
       ptx::tc_fence_before();
       __syncwarp();
@@ -714,12 +797,12 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 constexpr int kMaxDevices = 64;
+constexpr int kNumModes = 4;
 struct DeviceState {
   bool initialised = false;
   fs_status status = FS_ERR_UNSUPPORTED;
   int num_sms = 0;
-  int max_clusters[2][3] = {};  // [want_lse][log2 cluster size]: co-resident clusters
-  int max_pairs[2] = {};        // [want_lse]: co-resident CTA pairs of the pair kernel
+  int max_pairs[kNumModes] = {};  // co-resident CTA pairs of the pair kernel, per mode
 };
 
 std::mutex g_mu;
@@ -728,10 +811,8 @@ EncodeTiledFn g_encode = nullptr;
 thread_local const DeviceState* g_last_state = nullptr;  // set by device_setup
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
-constexpr int log2_cluster(int c) { return c == 1 ? 0 : c == 2 ? 1 : 2; }
-
 cudaLaunchConfig_t launch_config(int cluster, cudaLaunchAttribute* attr, cudaStream_t stream,
-                                 size_t smem = kSmemBytes) {
+                                 size_t smem) {
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
@@ -741,74 +822,51 @@ cudaLaunchConfig_t launch_config(int cluster, cudaLaunchAttribute* attr, cudaStr
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = cluster > 1 ? 1 : 0;
   return cfg;
 }
 
-// Opt one stage-1 variant into its shared memory and record how many of its
-// clusters fit on the device at once (the persistent grid size).
-template <bool kWantLse, int kCluster>
-bool prepare_variant(DeviceState& st, int sms) {
-  auto kern = stage1_kernel<kWantLse, kCluster>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes)) !=
-      cudaSuccess)
+// Opt both stage-1 kernels of one epilogue mode into their shared memory and
+// record how many CTA pairs fit on the device at once (the pair kernel's
+// persistent grid).
+template <int kMode>
+bool prepare_mode(DeviceState& st, int sms) {
+  if (cudaFuncSetAttribute(stage1_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(kSmemBytes)) != cudaSuccess)
     return false;
-  int n = sms / kCluster;
-  if (kCluster > 1) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 0) !=
-        cudaSuccess)
-      return false;
-    cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = launch_config(kCluster, attr, nullptr);
-    cfg.gridDim = dim3(unsigned(n * kCluster), 1, 1);
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) return false;
-  }
-  st.max_clusters[kWantLse ? 1 : 0][log2_cluster(kCluster)] = n;
-  return true;
-}
-
-template <bool kWantLse>
-bool prepare_pair_variant(DeviceState& st, int sms) {
-  auto kern = stage1_pair_kernel<kWantLse>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  auto pk = stage1_pair_kernel<kMode>;
+  if (cudaFuncSetAttribute(pk, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            int(kPairSmemBytes)) != cudaSuccess)
     return false;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = launch_config(2, attr, nullptr, kPairSmemBytes);
   cfg.gridDim = dim3(unsigned((sms / 2) * 2), 1, 1);
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) return false;
-  st.max_pairs[kWantLse ? 1 : 0] = n;
+  if (cudaOccupancyMaxActiveClusters(&n, pk, &cfg) != cudaSuccess || n < 1) return false;
+  st.max_pairs[kMode] = n;
   return true;
 }
 
-template <bool kWantLse>
-fs_status launch_stage1_pair(const CUtensorMap& tmap_h, const CUtensorMap& tmap_w,
-                             const Stage1Params& p, int max_pairs, cudaStream_t stream) {
-  const int n_units = int((int64_t(p.V) + kBlockN - 1) / kBlockN) *
-                      int((int64_t(p.B) + 2 * kBlockM - 1) / (2 * kBlockM));
-  const int pairs = n_units < max_pairs ? n_units : max_pairs;
+template <int kMode>
+fs_status launch_mode(bool pair, const CUtensorMap& tmap_h, const CUtensorMap& tmap_w,
+                      const Stage1Params& p, const DeviceState& ds, cudaStream_t stream) {
+  const int n_vt = int((int64_t(p.V) + kBlockN - 1) / kBlockN);
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = launch_config(2, attr, stream, kPairSmemBytes);
-  cfg.gridDim = dim3(unsigned(pairs * 2), 1, 1);
-  if (cudaLaunchKernelEx(&cfg, stage1_pair_kernel<kWantLse>, tmap_h, tmap_w, p) != cudaSuccess) {
-    cudaGetLastError();
-    return FS_ERR_CUDA;
+  cudaError_t err;
+  if (pair) {
+    const int n_units = n_vt * int((int64_t(p.B) + 2 * kBlockM - 1) / (2 * kBlockM));
+    const int pairs = n_units < ds.max_pairs[kMode] ? n_units : ds.max_pairs[kMode];
+    cudaLaunchConfig_t cfg = launch_config(2, attr, stream, kPairSmemBytes);
+    cfg.gridDim = dim3(unsigned(pairs * 2), 1, 1);
+    err = cudaLaunchKernelEx(&cfg, stage1_pair_kernel<kMode>, tmap_h, tmap_w, p);
+  } else {
+    const int n_units = n_vt * p.n_mt;
+    const int grid = n_units < ds.num_sms ? n_units : ds.num_sms;
+    cudaLaunchConfig_t cfg = launch_config(1, attr, stream, kSmemBytes);
+    cfg.gridDim = dim3(unsigned(grid), 1, 1);
+    err = cudaLaunchKernelEx(&cfg, stage1_kernel<kMode>, tmap_h, tmap_w, p);
   }
-  return FS_OK;
-}
-
-template <bool kWantLse, int kCluster>
-fs_status launch_stage1(const CUtensorMap& tmap_h, const CUtensorMap& tmap_w, Stage1Params p,
-                        int max_clusters, cudaStream_t stream) {
-  p.n_mgroups = (p.n_mt + kCluster - 1) / kCluster;
-  p.n_cunits = int32_t((int64_t(p.V) + kBlockN - 1) / kBlockN) * p.n_mgroups;
-  const int clusters = p.n_cunits < max_clusters ? p.n_cunits : max_clusters;
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = launch_config(kCluster, attr, stream);
-  cfg.gridDim = dim3(unsigned(clusters * kCluster), 1, 1);
-  if (cudaLaunchKernelEx(&cfg, stage1_kernel<kWantLse, kCluster>, tmap_h, tmap_w, p) !=
-      cudaSuccess) {
+  if (err != cudaSuccess) {
     cudaGetLastError();
     return FS_ERR_CUDA;
   }
@@ -836,10 +894,8 @@ fs_status device_setup(int* num_sms) {
       st.status = FS_ERR_UNSUPPORTED;
     } else {
       st.status = FS_OK;
-      if (!prepare_variant<false, 1>(st, sms) || !prepare_variant<true, 1>(st, sms) ||
-          !prepare_variant<false, 2>(st, sms) || !prepare_variant<true, 2>(st, sms) ||
-          !prepare_variant<false, 4>(st, sms) || !prepare_variant<true, 4>(st, sms) ||
-          !prepare_pair_variant<false>(st, sms) || !prepare_pair_variant<true>(st, sms)) {
+      if (!prepare_mode<kModeSample>(st, sms) || !prepare_mode<kModeLse>(st, sms) ||
+          !prepare_mode<kModeTop4>(st, sms) || !prepare_mode<kModeTop16>(st, sms)) {
         cudaGetLastError();
         st.status = FS_ERR_CUDA;
       }
@@ -889,6 +945,10 @@ using namespace fs;
 namespace fs {
 fs_status launch_row_lse(const float* tile_lse, const float* temperature, int64_t B,
                          int64_t n_tiles, float* out_lse, cudaStream_t stream);
+// Defined in fs_merge.cu: each row's K best of its per-tile top-K candidates.
+fs_status launch_topk_reduce(const float* cand_score, const int32_t* cand_idx, int64_t B,
+                             int64_t n_cand, int64_t K, int64_t* out_idx, float* out_score,
+                             cudaStream_t stream);
 }
 
 extern "C" int64_t fs_num_tiles(int64_t V) { return V <= 0 ? 0 : (V + kTileV - 1) / kTileV; }
@@ -914,42 +974,36 @@ extern "C" const char* fs_status_string(int status) {
   }
 }
 
-extern "C" fs_status fs_sample(const fs_sample_args* a, void* stream_ptr) {
+namespace fs {
+namespace {
+
+// Checks shared by every sampling entry point: the inputs of fs_sample_args.
+fs_status check_inputs(const fs_sample_args* a) {
   if (a == nullptr) return FS_ERR_INVALID_ARG;
   const int64_t B = a->B, d = a->d, V = a->V;
   if (!a->H || !a->W) return FS_ERR_INVALID_ARG;
-  if (!a->out_idx && !a->out_tile_max) return FS_ERR_INVALID_ARG;
   if (B < 1 || B > 65535 || d < 1 || V < 1 || V > int64_t(0x7FFFFFFF)) return FS_ERR_INVALID_ARG;
   if (d > int64_t(0x7FFFFFFF) - kBlockK) return FS_ERR_INVALID_ARG;
   if (a->ldh < d || a->ldw < d || a->ldh % 8 != 0 || a->ldw % 8 != 0) return FS_ERR_INVALID_ARG;
   if (!aligned(a->H, 16) || !aligned(a->W, 16)) return FS_ERR_INVALID_ARG;
-  if (a->out_idx && !aligned(a->out_idx, 8)) return FS_ERR_INVALID_ARG;
   if (a->temperature && !aligned(a->temperature, 4)) return FS_ERR_INVALID_ARG;
   if (a->seeds && !aligned(a->seeds, 8)) return FS_ERR_INVALID_ARG;
   if (a->vocab_mask && (!aligned(a->vocab_mask, 4) || a->mask_ld < (V + 31) / 32))
     return FS_ERR_INVALID_ARG;
-  if ((a->out_tile_max == nullptr) != (a->out_tile_idx == nullptr)) return FS_ERR_INVALID_ARG;
-  if (a->out_tile_max && (!aligned(a->out_tile_max, 4) || !aligned(a->out_tile_idx, 4)))
-    return FS_ERR_INVALID_ARG;
-  if (a->out_tile_lse && (!aligned(a->out_tile_lse, 4) || !a->out_tile_max))
-    return FS_ERR_INVALID_ARG;
   if (a->vocab_offset < 0 || a->vocab_offset % 4 != 0 ||
       a->vocab_offset + V > int64_t(0x7FFFFFFF))
     return FS_ERR_INVALID_ARG;
-  if (a->out_max && (!a->out_idx || !aligned(a->out_max, 4))) return FS_ERR_INVALID_ARG;
-  if (a->out_lse && (!a->out_tile_lse || !aligned(a->out_lse, 4))) return FS_ERR_INVALID_ARG;
+  return FS_OK;
+}
 
-  const int64_t n_tiles = fs_num_tiles(V);
-  if (a->out_idx != nullptr) {
-    const size_t need = fs_workspace_size(B, V);
-    if (!a->workspace || a->workspace_bytes < need || !aligned(a->workspace, 256))
-      return FS_ERR_WORKSPACE;
-  }
-
+// Encode the tensor maps, fill the kernel parameters and launch the stage-1
+// kernel of `mode` (single CTAs, or CTA pairs for an even number of 128-row
+// batch blocks).  `p` arrives with the output pointers set.
+fs_status run_stage1(const fs_sample_args* a, int mode, Stage1Params& p, cudaStream_t stream) {
   int num_sms = 0;
   const fs_status st = device_setup(&num_sms);
   if (st != FS_OK) return st;
-
+  const int64_t B = a->B, d = a->d, V = a->V;
   // H box: only the rows that exist (rounded up to the 8-row swizzle atom);
   // the MMA's remaining A rows hold stale data and only feed accumulator rows
   // that are never read.
@@ -958,25 +1012,19 @@ extern "C" fs_status fs_sample(const fs_sample_args* a, void* stream_ptr) {
   // An even number of 128-row batch blocks: CTA pairs with M = 256 MMAs, each
   // CTA holding half of the W slice (six 32 KB stages).  Otherwise single CTAs
   // with M = 128 and the whole slice (four 48 KB stages); with an odd number of
-  // batch blocks above one, clusters of two CTAs would leave half a pair idle,
-  // so those stay single too.
+  // batch blocks above one, pairs would leave half a pair idle.
   const bool pair = n_mt > 1 && n_mt % 2 == 0;
-  const int cluster = 1;
   CUtensorMap tmap_h, tmap_w;
   if (!encode_2d(&tmap_h, a->H, uint64_t(d), uint64_t(B), uint64_t(a->ldh) * 2u, kBlockK,
                  h_rows) ||
       !encode_2d(&tmap_w, a->W, uint64_t(d), uint64_t(V), uint64_t(a->ldw) * 2u, kBlockK,
-                 uint32_t(pair ? kBlockN / 2 : kBlockN / cluster)))
+                 uint32_t(pair ? kBlockN / 2 : kBlockN)))
     return FS_ERR_INVALID_ARG;
-
-  Stage1Params p;
   p.B = int32_t(B);
   p.V = int32_t(V);
   p.d = int32_t(d);
-  p.n_tiles = int32_t(n_tiles);
+  p.n_tiles = int32_t(fs_num_tiles(V));
   p.n_mt = int32_t(n_mt);
-  p.n_mgroups = 0;  // set per variant at launch
-  p.n_cunits = 0;
   p.n_kb = int32_t((d + kBlockK - 1) / kBlockK);
   p.temperature = a->temperature;
   p.mask = a->vocab_mask;
@@ -984,35 +1032,87 @@ extern "C" fs_status fs_sample(const fs_sample_args* a, void* stream_ptr) {
   p.seeds = a->seeds;
   p.seed = a->seed;
   p.offset = a->offset;
+  p.vocab_offset = int32_t(a->vocab_offset);
+  p.wait_limit_ns = kWaitLimitNs;
+  p.h_box_rows = h_rows;
+  const DeviceState& ds = *g_last_state;
+  switch (mode) {
+    case kModeSample: return launch_mode<kModeSample>(pair, tmap_h, tmap_w, p, ds, stream);
+    case kModeLse: return launch_mode<kModeLse>(pair, tmap_h, tmap_w, p, ds, stream);
+    case kModeTop4: return launch_mode<kModeTop4>(pair, tmap_h, tmap_w, p, ds, stream);
+    default: return launch_mode<kModeTop16>(pair, tmap_h, tmap_w, p, ds, stream);
+  }
+}
+
+}  // namespace
+}  // namespace fs
+
+extern "C" fs_status fs_sample(const fs_sample_args* a, void* stream_ptr) {
+  const fs_status chk = check_inputs(a);
+  if (chk != FS_OK) return chk;
+  const int64_t B = a->B, V = a->V;
+  if (!a->out_idx && !a->out_tile_max) return FS_ERR_INVALID_ARG;
+  if (a->out_idx && !aligned(a->out_idx, 8)) return FS_ERR_INVALID_ARG;
+  if ((a->out_tile_max == nullptr) != (a->out_tile_idx == nullptr)) return FS_ERR_INVALID_ARG;
+  if (a->out_tile_max && (!aligned(a->out_tile_max, 4) || !aligned(a->out_tile_idx, 4)))
+    return FS_ERR_INVALID_ARG;
+  if (a->out_tile_lse && (!aligned(a->out_tile_lse, 4) || !a->out_tile_max))
+    return FS_ERR_INVALID_ARG;
+  if (a->out_max && (!a->out_idx || !aligned(a->out_max, 4))) return FS_ERR_INVALID_ARG;
+  if (a->out_lse && (!a->out_tile_lse || !aligned(a->out_lse, 4))) return FS_ERR_INVALID_ARG;
+  if (a->out_idx != nullptr) {
+    const size_t need = fs_workspace_size(B, V);
+    if (!a->workspace || a->workspace_bytes < need || !aligned(a->workspace, 256))
+      return FS_ERR_WORKSPACE;
+  }
+  Stage1Params p = {};
   p.tile_max = a->out_tile_max;
   p.tile_idx = a->out_tile_idx;
   p.tile_lse = a->out_tile_lse;
   p.out_idx = a->out_idx;
   p.out_max = a->out_max;
-  p.vocab_offset = int32_t(a->vocab_offset);
   p.ticket = a->out_idx ? static_cast<uint32_t*>(a->workspace) : nullptr;
   p.row_keys = a->out_idx ? reinterpret_cast<unsigned long long*>(
                                 static_cast<uint8_t*>(a->workspace) + kKeysOffset)
                           : nullptr;
-  p.wait_limit_ns = kWaitLimitNs;
-  p.h_box_rows = h_rows;
-
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
-  const DeviceState& ds = *g_last_state;
-  const bool lse = a->out_tile_lse != nullptr;
-  const int mc = ds.max_clusters[lse ? 1 : 0][log2_cluster(cluster)];
-  fs_status lst;
-  if (pair)
-    lst = lse ? launch_stage1_pair<true>(tmap_h, tmap_w, p, ds.max_pairs[1], stream)
-              : launch_stage1_pair<false>(tmap_h, tmap_w, p, ds.max_pairs[0], stream);
-  else if (cluster == 2)
-    lst = lse ? launch_stage1<true, 2>(tmap_h, tmap_w, p, mc, stream)
-              : launch_stage1<false, 2>(tmap_h, tmap_w, p, mc, stream);
-  else
-    lst = lse ? launch_stage1<true, 1>(tmap_h, tmap_w, p, mc, stream)
-              : launch_stage1<false, 1>(tmap_h, tmap_w, p, mc, stream);
+  const fs_status lst = run_stage1(a, a->out_tile_lse ? kModeLse : kModeSample, p, stream);
   if (lst != FS_OK || a->out_lse == nullptr) return lst;
-  return launch_row_lse(a->out_tile_lse, a->temperature, B, n_tiles, a->out_lse, stream);
+  return launch_row_lse(a->out_tile_lse, a->temperature, B, fs_num_tiles(V), a->out_lse, stream);
+}
+
+extern "C" size_t fs_topk_workspace_size(int64_t B, int64_t V, int64_t K) {
+  if (B <= 0 || V <= 0 || K < 1 || K > FS_TOPK_MAX) return 0;
+  const size_t cap = K <= 4 ? 4u : 16u;
+  const size_t bytes = size_t(B) * size_t(fs_num_tiles(V)) * cap * 8u;
+  return (bytes + 255u) & ~size_t(255u);
+}
+
+extern "C" fs_status fs_sample_topk(const fs_sample_args* a, int64_t K, int64_t* out_topk_idx,
+                                    float* out_topk_score, void* stream_ptr) {
+  const fs_status chk = check_inputs(a);
+  if (chk != FS_OK) return chk;
+  const int64_t B = a->B, V = a->V;
+  if (K < 1 || K > FS_TOPK_MAX || !out_topk_idx || !aligned(out_topk_idx, 8) ||
+      (out_topk_score && !aligned(out_topk_score, 4)))
+    return FS_ERR_INVALID_ARG;
+  if (a->out_idx || a->out_tile_max || a->out_tile_idx || a->out_tile_lse || a->out_max ||
+      a->out_lse)
+    return FS_ERR_INVALID_ARG;
+  const size_t need = fs_topk_workspace_size(B, V, K);
+  if (!a->workspace || a->workspace_bytes < need || !aligned(a->workspace, 256))
+    return FS_ERR_WORKSPACE;
+  const int cap = K <= 4 ? 4 : 16;
+  const int64_t n_cand = fs_num_tiles(V) * cap;
+  Stage1Params p = {};
+  p.topk_score = static_cast<float*>(a->workspace);
+  p.topk_idx = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(a->workspace) +
+                                          size_t(B) * size_t(n_cand) * 4u);
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  const fs_status lst = run_stage1(a, cap == 4 ? kModeTop4 : kModeTop16, p, stream);
+  if (lst != FS_OK) return lst;
+  return launch_topk_reduce(p.topk_score, p.topk_idx, B, n_cand, K, out_topk_idx,
+                            out_topk_score, stream);
 }
 
 // ---- allocation-free variant ---------------------------------------------

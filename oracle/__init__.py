@@ -166,6 +166,29 @@ class Oracle:
         return out
 
 
+def topk_from_scores(scores, K):
+    """The ids of the K largest scores of each row, best first, ties to the
+    lower id (a library sort is the step); -1 / -inf past the finite count."""
+    scores = np.asarray(scores, dtype=np.float64)
+    n, V = scores.shape
+    idx = np.full((n, K), -1, dtype=np.int64)
+    val = np.full((n, K), -np.inf)
+    for r in range(n):
+        order = np.lexsort((np.arange(V), -scores[r]))  # score desc, then id asc
+        keep = [v for v in order[:K] if np.isfinite(scores[r, v])]
+        idx[r, :len(keep)] = keep
+        val[r, :len(keep)] = scores[r, keep]
+    return idx, val
+
+
+def sample_topk(o, H, W, K, **kw):
+    """K draws without replacement per row (the K largest noisy scores):
+    returns (ids [n, K], scores [n, K], the oracle's sample dict)."""
+    ref = o.sample(H, W, want_scores=True, **kw)
+    idx, val = topk_from_scores(ref["scores"], K)
+    return idx, val, ref
+
+
 _default: Oracle | None = None
 
 

@@ -383,6 +383,44 @@ def pin_masked_distribution(o):
     assert pval > P_MIN, (stat, dof, pval)
 
 
+def pin_topk_first_is_sample_and_greedy_sort(o):
+    """The first of the K largest scores is the sample; for greedy rows the K
+    are numpy's descending sort of the fp64 logits (lowest id on ties)."""
+    from oracle import sample_topk
+    B, d, V = 5, 24, 700
+    H, W = make_problem(B, d, V, seed=41)
+    W[650] = W[3]  # an exact tie
+    T = np.array([0.8, 1.0, 0.0, 1.3, 0.0], np.float32)
+    idx, val, ref = sample_topk(o, H, W, 6, temperature=T, seed=2, offset=3)
+    assert np.array_equal(idx[:, 0], ref["idx"])
+    assert np.all(np.diff(val, axis=1) <= 0)
+    L = ref_logits(H, W)
+    for b in (2, 4):
+        order = np.lexsort((np.arange(V), -L[b]))[:6]
+        assert np.array_equal(idx[b], order)
+
+
+def pin_topk_plackett_luce(o):
+    """Two draws without replacement: P(first = i, second = j) =
+    p_i p_j / (1 - p_i) with p = softmax(l / T) (chi-square over ordered pairs)."""
+    from oracle import topk_from_scores
+    V, d, T, n = 6, 8, 1.0, 12000
+    H, W = make_problem(1, d, V, seed=42)
+    p = scipy.special.softmax(ref_logits(H, W)[0] / T)
+    temp = np.full(1, T, np.float32)
+    counts = np.zeros((V, V))
+    for off in range(n):
+        r = o.sample(H, W, temperature=temp, seed=5, offset=off, want_scores=True)
+        ij, _ = topk_from_scores(r["scores"], 2)
+        counts[ij[0, 0], ij[0, 1]] += 1
+    want = np.array([[p[i] * p[j] / (1 - p[i]) if i != j else 0.0 for j in range(V)]
+                     for i in range(V)])
+    off_diag = ~np.eye(V, dtype=bool)
+    assert counts[~off_diag].sum() == 0
+    _, _, pval = chi_square_gof(counts[off_diag], want[off_diag])
+    assert pval > P_MIN, pval
+
+
 ALL_PINS = [
     pin_philox_kat,
     pin_uniform_map,
@@ -401,4 +439,6 @@ ALL_PINS = [
     pin_max_stability,
     pin_group_merges,
     pin_merge_uniform,
+    pin_topk_first_is_sample_and_greedy_sort,
+    pin_topk_plackett_luce,
 ]

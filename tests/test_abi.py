@@ -32,7 +32,8 @@ def test_header_declares_entry_points():
     names = declared_functions()
     for want in ("fs_sample", "fs_workspace_size", "fs_num_tiles", "fs_status_string",
                  "fs_gumbel_noise", "fs_last_device_error", "fs_group_merge", "fs_online_merge",
-                 "fs_sample_noalloc", "fs_wait_timeout_selftest"):
+                 "fs_sample_noalloc", "fs_wait_timeout_selftest", "fs_sample_topk",
+                 "fs_topk_workspace_size"):
         assert want in names
 
 
@@ -140,3 +141,22 @@ def test_merge_bad_arguments(lib):
     assert om(None, L, z, L, 4, 0, None, 0, 0, None) == 1
     assert om(z, L, z, L, 0, 0, None, 0, 0, None) == 1
     assert om(z, L, z, L, 4, 2**33, None, 0, 0, None) == 1
+
+
+def test_topk_workspace_and_bad_arguments(lib):
+    import lm_head_gumbel_gb300 as fs
+    assert fs.fs_topk_workspace_size(4, 4096, 1) == 4 * 32 * 4 * 8
+    assert fs.fs_topk_workspace_size(4, 4096, 5) == 4 * 32 * 16 * 8
+    assert fs.fs_topk_workspace_size(4, 4096, 0) == 0
+    assert fs.fs_topk_workspace_size(4, 4096, 17) == 0
+    o = ctypes.c_void_p(0x90000)
+    good = dict(out_tile_max=None, out_tile_idx=None, out_idx=None, workspace=0x100000,
+                workspace_bytes=1 << 20)
+    f = lib.fs_sample_topk
+    assert f(ctypes.byref(_args(**good)), 0, o, None, None) == 1         # K < 1
+    assert f(ctypes.byref(_args(**good)), 17, o, None, None) == 1        # K > max
+    assert f(ctypes.byref(_args(**good)), 4, None, None, None) == 1      # no output
+    assert f(ctypes.byref(_args(**dict(good, out_idx=0x30000))), 4, o, None, None) == 1
+    assert f(ctypes.byref(_args(**dict(good, workspace_bytes=100))), 4, o, None, None) == 5
+    assert f(ctypes.byref(_args(**dict(good, workspace=None))), 4, o, None, None) == 5
+    assert f(None, 4, o, None, None) == 1

@@ -1,0 +1,137 @@
+"""K draws without replacement (Gumbel-top-k) on the GPU, against the oracle.
+
+The ids of the K largest noisy scores per row, best first: the first equals
+fs_sample's draw; the list matches the oracle where the oracle's consecutive
+score gaps exceed the parity gate; the ordered pairs follow the
+Plackett-Luce law p_i p_j / (1 - p_i) (chi-square); masked ids never appear
+and short rows pad with -1.
+"""
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import lm_head_gumbel_gb300 as fs
+from lm_head_gumbel_gb300 import workloads as wl
+import oracle
+from oracle import merge, parity, sample_topk
+from gpu_cases import assert_no_device_error, make_problem
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    fs.load_library()
+    yield
+    assert_no_device_error()
+
+
+def device_topk(p, K, *, seed=7, offset=0):
+    B = p["H"].shape[0]
+    score = torch.empty((B, K), dtype=torch.float32, device="cuda")
+    idx = fs.fs_sample_topk(p["H"], p["W"], K, temperature=p["temperature"],
+                            vocab_mask=p["vocab_mask"], seeds=p["seeds"], seed=seed,
+                            offset=offset, out_topk_score=score)
+    torch.cuda.synchronize()
+    return idx.cpu().numpy(), score.cpu().numpy()
+
+
+def check_against_oracle(p, K, idx, score, rows=None, *, seed=7, offset=0):
+    o = oracle.default()
+    ridx, rval, ref = sample_topk(
+        o, wl.bf16_bits(p["H"]), wl.bf16_bits(p["W"]), K + 1,
+        temperature=p["temperature"].cpu().numpy(),
+        mask=None if p["vocab_mask"] is None else wl.u32_bits(p["vocab_mask"]),
+        seeds=None if p["seeds"] is None else wl.u64_bits(p["seeds"]), seed=seed,
+        offset=offset, rows=rows)
+    sel = ref["rows"]
+    n_exact = 0
+    for r, b in enumerate(sel):
+        with np.errstate(invalid="ignore"):
+            gaps = -np.diff(rval[r])  # s(j) - s(j+1), j = 0..K-1 (nan past the count)
+        for j in range(K):
+            if ridx[r, j] < 0:
+                assert idx[b, j] == -1
+                continue
+            assert abs(score[b, j] - rval[r, j]) <= parity.TOL_MAX, (b, j)
+            left_ok = j == 0 or gaps[j - 1] > parity.GAP
+            if left_ok and gaps[j] > parity.GAP:
+                assert idx[b, j] == ridx[r, j], (b, j)
+                n_exact += 1
+    return n_exact
+
+
+@pytest.mark.parametrize("K", [1, 3, 4, 8, 16])
+def test_topk_matches_oracle_and_first_is_the_sample(K):
+    p = make_problem(20, 128, 3000, T="row-uniform", per_row_seeds=True, mask_frac=0.03,
+                     seed=40 + K)
+    idx, score = device_topk(p, K, offset=3)
+    one = fs.fs_sample(p["H"], p["W"], temperature=p["temperature"], vocab_mask=p["vocab_mask"],
+                       seeds=p["seeds"], seed=7, offset=3)
+    torch.cuda.synchronize()
+    assert np.array_equal(idx[:, 0], one.cpu().numpy())
+    assert np.all(np.diff(score, axis=1) <= 0)
+    for b in range(idx.shape[0]):  # distinct ids
+        got = idx[b][idx[b] >= 0]
+        assert len(set(got.tolist())) == len(got)
+    assert check_against_oracle(p, K, idx, score, offset=3) > 0.8 * 20 * K
+
+
+def test_topk_short_rows_and_masks():
+    p = make_problem(4, 64, 1000, T=1.0, mask_frac=0.02, seed=50)
+    m = p["vocab_mask"]
+    m[1, :] = 0
+    m[1, 3] = 0b1011  # three allowed ids: 96, 97, 99
+    m[2, :] = 0       # nothing allowed
+    idx, score = device_topk(p, 8, offset=1)
+    assert set(idx[1, :3].tolist()) == {96, 97, 99} and np.all(idx[1, 3:] == -1)
+    assert np.all(np.isneginf(score[1, 3:]))
+    assert np.all(idx[2] == -1)
+    mm = m.cpu().numpy().view(np.uint32)
+    for b in (0, 3):
+        bits = (mm[b, idx[b] // 32] >> (idx[b] % 32)) & 1
+        assert np.all(bits == 1)
+    check_against_oracle(p, 8, idx, score, offset=1)
+
+
+def test_topk_pairs_follow_plackett_luce():
+    V, d, T, n = 8, 16, 1.0, 6000
+    p = make_problem(1, d, V, T=T, seed=51)
+    probs = scipy.special.softmax(
+        oracle.default().logits(wl.bf16_bits(p["H"]), wl.bf16_bits(p["W"]))[0] / T)
+    out = torch.empty((n, 2), dtype=torch.int64, device="cuda")
+    ws = torch.empty(fs.fs_topk_workspace_size(1, V, 2), dtype=torch.uint8, device="cuda")
+    for off in range(n):
+        fs.fs_sample_topk(p["H"], p["W"], 2, temperature=p["temperature"], seed=11, offset=off,
+                          out_topk_idx=out[off:off + 1], workspace=ws)
+    torch.cuda.synchronize()
+    pairs = out.cpu().numpy()
+    counts = np.zeros((V, V))
+    np.add.at(counts, (pairs[:, 0], pairs[:, 1]), 1)
+    want = np.array([[probs[i] * probs[j] / (1 - probs[i]) if i != j else 0.0
+                      for j in range(V)] for i in range(V)])
+    off_diag = ~np.eye(V, dtype=bool)
+    assert counts[~off_diag].sum() == 0
+    _, _, pval = merge.chi_square_gof(counts[off_diag], want[off_diag])
+    assert pval > 1e-3, pval
+
+
+@pytest.mark.parametrize("B,K", [(64, 8), (256, 16)])
+def test_topk_full_size_head(B, K):
+    """Qwen3-8B-shaped head (d=4096, V=151936): the single-CTA kernel (B=64)
+    and the CTA-pair kernel (B=256) in top-K mode; sampled rows against the
+    oracle, every row's first id against fs_sample."""
+    w = wl.WORKLOADS["qwen3-8b"]
+    W = wl.make_weights(w.d, w.V, seed=77, device="cuda")
+    p = make_problem(B, w.d, w.V, T="row-uniform", per_row_seeds=True, seed=B, W=W)
+    idx, score = device_topk(p, K, offset=2)
+    one = fs.fs_sample(p["H"], W, temperature=p["temperature"], seeds=p["seeds"], offset=2,
+                       seed=7)
+    torch.cuda.synchronize()
+    assert np.array_equal(idx[:, 0], one.cpu().numpy())
+    assert np.all((idx >= 0) & (idx < w.V))
+    rows = [0, B // 3, B - 1]
+    assert check_against_oracle(p, K, idx, score, rows=rows, offset=2) >= len(rows) * K * 0.6
