@@ -189,7 +189,6 @@ __global__ void __launch_bounds__(kTopkThreads)
   }
   __shared__ float ws[kTopkThreads / 32];
   __shared__ int32_t wi[kTopkThreads / 32];
-  __shared__ float win_s;
   __shared__ int32_t win_i;
   for (int j = 0; j < K; ++j) {
     float bs = ls[0];
@@ -214,7 +213,6 @@ __global__ void __launch_bounds__(kTopkThreads)
           bs = ws[w];
           bi = wi[w];
         }
-      win_s = bs;
       win_i = bi;
       out_idx[int64_t(row) * K + j] = bi;
       if (out_score != nullptr) out_score[int64_t(row) * K + j] = bi >= 0 ? bs : -INFINITY;
