@@ -63,10 +63,12 @@ def test_tiny(T):
 @pytest.mark.parametrize("B,d,V", [
     (1, 8, 1), (1, 8, 2), (3, 72, 100), (1, 264, 1000), (5, 64, 129), (2, 136, 4097),
     (7, 200, 255), (33, 96, 257), (129, 64, 640), (130, 128, 3000), (300, 64, 1100),
+    (256, 72, 100), (256, 64, 1), (260, 64, 300), (512, 40, 700), (511, 64, 1300),
 ])
 def test_ragged_shapes(B, d, V):
-    """Odd B (several 128-row blocks), d not a multiple of 64, V with a
-    ragged last tile and a ragged last 256-id unit."""
+    """Odd B (several 128-row blocks, CTA pairs for even block counts), d not
+    a multiple of 64, V with a ragged last tile and a ragged last 256-id unit
+    (including a vocabulary smaller than one pair's half slice)."""
     p = make_problem(B, d, V, T=0.9, seed=B + d + V)
     dev = run_device(p, seed=3, offset=5)
     compare(p, dev, seed=3, offset=5, scores=True)
