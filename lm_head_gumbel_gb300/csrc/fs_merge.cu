@@ -150,41 +150,46 @@ __device__ __forceinline__ bool precedes(float as, int32_t ai, float bs, int32_t
   return ai >= 0 && (bi < 0 || as > bs || (as == bs && ai < bi));
 }
 
-constexpr int kTopkThreads = 128;
-constexpr int kTopkCap = FS_TOPK_MAX;
+constexpr int kTopkThreads = 256;
 
 // Each row's K best of its per-tile candidates (Gumbel-top-k: K draws without
-// replacement, in draw order).  One block per row: every thread keeps the
-// kTopkCap best of its share, then K rounds pick the best remaining head.
+// replacement, in draw order).  One block per row.  Every tile's KC
+// candidates arrive sorted best first, so a thread walks each of its tiles
+// only until a candidate no longer makes its own KC-best list; then K rounds
+// pick the best remaining head across the block.
+template <int KC>
 __global__ void __launch_bounds__(kTopkThreads)
     topk_reduce_kernel(const float* __restrict__ cand_score,
-                       const int32_t* __restrict__ cand_idx, int64_t n_cand, int32_t K,
+                       const int32_t* __restrict__ cand_idx, int32_t n_tiles, int32_t K,
                        int64_t* __restrict__ out_idx, float* __restrict__ out_score) {
   const int row = blockIdx.x;
-  const float* cs = cand_score + int64_t(row) * n_cand;
-  const int32_t* ci = cand_idx + int64_t(row) * n_cand;
-  float ls[kTopkCap];
-  int32_t li[kTopkCap];
+  const int64_t base = int64_t(row) * n_tiles * KC;
+  float ls[KC];
+  int32_t li[KC];
 #pragma unroll
-  for (int q = 0; q < kTopkCap; ++q) {
+  for (int q = 0; q < KC; ++q) {
     ls[q] = -INFINITY;
     li[q] = -1;
   }
-  for (int64_t c = threadIdx.x; c < n_cand; c += kTopkThreads) {
-    const float sc = cs[c];
-    const int32_t ic = ci[c];
-    if (!precedes(sc, ic, ls[kTopkCap - 1], li[kTopkCap - 1])) continue;
-    ls[kTopkCap - 1] = sc;
-    li[kTopkCap - 1] = ic;
+  for (int t = threadIdx.x; t < n_tiles; t += kTopkThreads) {
+    const float* ts = cand_score + base + int64_t(t) * KC;
+    const int32_t* ti = cand_idx + base + int64_t(t) * KC;
+    for (int q = 0; q < KC; ++q) {
+      const float sc = ts[q];
+      const int32_t ic = ti[q];
+      if (!precedes(sc, ic, ls[KC - 1], li[KC - 1])) break;  // the rest are worse
+      ls[KC - 1] = sc;
+      li[KC - 1] = ic;
 #pragma unroll
-    for (int q = kTopkCap - 1; q > 0; --q) {
-      const bool up = precedes(ls[q], li[q], ls[q - 1], li[q - 1]);
-      const float a = ls[q], b = ls[q - 1];
-      const int32_t ia = li[q], ib = li[q - 1];
-      ls[q - 1] = up ? a : b;
-      ls[q] = up ? b : a;
-      li[q - 1] = up ? ia : ib;
-      li[q] = up ? ib : ia;
+      for (int u = KC - 1; u > 0; --u) {
+        const bool up = precedes(ls[u], li[u], ls[u - 1], li[u - 1]);
+        const float a = ls[u], b = ls[u - 1];
+        const int32_t ia = li[u], ib = li[u - 1];
+        ls[u - 1] = up ? a : b;
+        ls[u] = up ? b : a;
+        li[u - 1] = up ? ia : ib;
+        li[u] = up ? ib : ia;
+      }
     }
   }
   __shared__ float ws[kTopkThreads / 32];
@@ -220,12 +225,12 @@ __global__ void __launch_bounds__(kTopkThreads)
     __syncthreads();
     if (li[0] >= 0 && li[0] == win_i) {  // this thread held the winner: pop it
 #pragma unroll
-      for (int q = 0; q < kTopkCap - 1; ++q) {
+      for (int q = 0; q < KC - 1; ++q) {
         ls[q] = ls[q + 1];
         li[q] = li[q + 1];
       }
-      ls[kTopkCap - 1] = -INFINITY;
-      li[kTopkCap - 1] = -1;
+      ls[KC - 1] = -INFINITY;
+      li[KC - 1] = -1;
     }
   }
 }
@@ -233,10 +238,14 @@ __global__ void __launch_bounds__(kTopkThreads)
 }  // namespace
 
 fs_status launch_topk_reduce(const float* cand_score, const int32_t* cand_idx, int64_t B,
-                             int64_t n_cand, int64_t K, int64_t* out_idx, float* out_score,
-                             cudaStream_t stream) {
-  topk_reduce_kernel<<<unsigned(B), kTopkThreads, 0, stream>>>(cand_score, cand_idx, n_cand,
-                                                               int32_t(K), out_idx, out_score);
+                             int64_t n_tiles, int64_t cap, int64_t K, int64_t* out_idx,
+                             float* out_score, cudaStream_t stream) {
+  if (cap == 4)
+    topk_reduce_kernel<4><<<unsigned(B), kTopkThreads, 0, stream>>>(
+        cand_score, cand_idx, int32_t(n_tiles), int32_t(K), out_idx, out_score);
+  else
+    topk_reduce_kernel<16><<<unsigned(B), kTopkThreads, 0, stream>>>(
+        cand_score, cand_idx, int32_t(n_tiles), int32_t(K), out_idx, out_score);
   return cudaGetLastError() == cudaSuccess ? FS_OK : FS_ERR_CUDA;
 }
 

@@ -19,7 +19,9 @@
 //             columns (one output tile); it reads its logits from tensor
 //             memory, scales by 1/T, masks, adds Philox Gumbel noise, and
 //             keeps the running (max, argmax) and optionally the log-sum-exp
-// Only (m_t, i_t[, L_t]) per (row, 128-id tile) leaves the chip.
+//             -- or, in the top-K modes, the best 4 or 16 (score, id)
+// Only (m_t, i_t[, L_t]) -- or the top-K list -- per (row, 128-id tile)
+// leaves the chip.
 //
 // Stage 2 ("Stage 2 (Reduction)") is fused: each tile winner is folded into a
 // per-row 64-bit key with an order-free atomic max, and the last CTA to finish
@@ -29,7 +31,6 @@
 
 #include <cmath>
 #include <cstdint>
-#include <cstring>
 #include <mutex>
 
 #include "fs_noise.cuh"
@@ -61,7 +62,7 @@ enum : int { kErrWaitTimeout = 1 };
 __device__ int g_error_word = 0;
 
 struct Stage1Params {
-  int32_t B, V, d;
+  int32_t B, V;
   int32_t n_tiles;   // ceil(V / 128)
   int32_t n_mt;      // ceil(B / 128)
   int32_t n_kb;      // ceil(d / 64)
@@ -947,8 +948,8 @@ fs_status launch_row_lse(const float* tile_lse, const float* temperature, int64_
                          int64_t n_tiles, float* out_lse, cudaStream_t stream);
 // Defined in fs_merge.cu: each row's K best of its per-tile top-K candidates.
 fs_status launch_topk_reduce(const float* cand_score, const int32_t* cand_idx, int64_t B,
-                             int64_t n_cand, int64_t K, int64_t* out_idx, float* out_score,
-                             cudaStream_t stream);
+                             int64_t n_tiles, int64_t cap, int64_t K, int64_t* out_idx,
+                             float* out_score, cudaStream_t stream);
 }
 
 extern "C" int64_t fs_num_tiles(int64_t V) { return V <= 0 ? 0 : (V + kTileV - 1) / kTileV; }
@@ -993,6 +994,9 @@ fs_status check_inputs(const fs_sample_args* a) {
   if (a->vocab_offset < 0 || a->vocab_offset % 4 != 0 ||
       a->vocab_offset + V > int64_t(0x7FFFFFFF))
     return FS_ERR_INVALID_ARG;
+  // The kernels count work units ((V / 256) x (B / 128)) in 32-bit integers.
+  if (((V + kBlockN - 1) / kBlockN) * ((B + kBlockM - 1) / kBlockM) > int64_t(0x7FFFFFFF))
+    return FS_ERR_INVALID_ARG;
   return FS_OK;
 }
 
@@ -1022,7 +1026,6 @@ fs_status run_stage1(const fs_sample_args* a, int mode, Stage1Params& p, cudaStr
     return FS_ERR_INVALID_ARG;
   p.B = int32_t(B);
   p.V = int32_t(V);
-  p.d = int32_t(d);
   p.n_tiles = int32_t(fs_num_tiles(V));
   p.n_mt = int32_t(n_mt);
   p.n_kb = int32_t((d + kBlockK - 1) / kBlockK);
@@ -1111,7 +1114,7 @@ extern "C" fs_status fs_sample_topk(const fs_sample_args* a, int64_t K, int64_t*
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   const fs_status lst = run_stage1(a, cap == 4 ? kModeTop4 : kModeTop16, p, stream);
   if (lst != FS_OK) return lst;
-  return launch_topk_reduce(p.topk_score, p.topk_idx, B, n_cand, K, out_topk_idx,
+  return launch_topk_reduce(p.topk_score, p.topk_idx, B, fs_num_tiles(V), cap, K, out_topk_idx,
                             out_topk_score, stream);
 }
 

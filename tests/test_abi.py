@@ -92,6 +92,7 @@ def _args(**kw):
     (dict(out_tile_lse=0x80000, out_tile_max=None, out_tile_idx=None), 1),
     (dict(vocab_offset=-4), 1), (dict(vocab_offset=6), 1), (dict(vocab_offset=2**31 - 4096), 1),
     (dict(out_max=0x90000, out_idx=None), 1), (dict(out_lse=0x90000), 1),
+    (dict(B=65535, V=2**31 - 1, d=8, ldh=8, ldw=8), 1),  # work units beyond 32 bits
     (dict(), 5),                                   # sampling without a workspace
     (dict(out_tile_max=None, out_tile_idx=None), 5),
     (dict(out_tile_max=None, out_tile_idx=None, workspace=0x70000, workspace_bytes=511), 5),
