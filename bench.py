@@ -90,8 +90,9 @@ def roofline(B, d, V, us, peaks, traffic=None, **kw):
 
 
 def kernel_source_hash():
+    """Hash of the sampling kernels' device code (host-only edits keep it)."""
     h = hashlib.sha256()
-    for rel in ("lm_head_gumbel_gb300/csrc/fs_sample.cu", "lm_head_gumbel_gb300/csrc/fs_ptx.cuh",
+    for rel in ("lm_head_gumbel_gb300/csrc/fs_kernels.cuh", "lm_head_gumbel_gb300/csrc/fs_ptx.cuh",
                 "lm_head_gumbel_gb300/csrc/fs_noise.cuh"):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())

@@ -11,7 +11,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIBRARY = os.path.join(PKG, "libfs.so")
 SOURCES = [os.path.join(CSRC, "fs_sample.cu"), os.path.join(CSRC, "fs_merge.cu")]
-DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("fs_ptx.cuh", "fs_noise.cuh")] + [
+DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("fs_kernels.cuh", "fs_ptx.cuh",
+                                                    "fs_noise.cuh")] + [
     os.path.join(INCLUDE, "fs_sample.h")]
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -1,0 +1,794 @@
+// fs_kernels.cuh -- the device code of fused LM-head + exact Gumbel-max sampling
+// on GB300 (sm_103a).  Included by fs_sample.cu only (it defines device
+// variables); the host side (argument checks, tensor maps, launches, the C ABI)
+// is there.
+//
+// Stage 1 (the aitrends.kr write-up on FlashSampling, "Stage 1 (Fused
+// Kernel)"; tomesphere abstract, "compute logits tile-by-tile on chip, add
+// Gumbel noise, keep only one maximizer per row and per vocabulary tile"):
+// a persistent, warp-specialised kernel.  For up to 128 rows (and odd numbers
+// of 128-row blocks) each work unit is a 128-row batch block x 256-id
+// vocabulary block of the logits l = H W^T, computed by one CTA; for an even
+// number of batch blocks, CTA pairs compute 256 x 256 units with cta_group::2
+// MMAs (stage1_pair_kernel below).  Single-CTA roles:
+//   warp 0    TMA producer: streams 64-wide K slices of W (256 x 64) and
+//             H (up to 128 x 64) into a 4-stage shared-memory ring (128-byte
+//             swizzle)
+//   warp 1    tcgen05 MMA issuer: M=128, N=256, K=16 bf16 MMAs accumulate the
+//             unit's logits in tensor memory (fp32, 256 columns); two
+//             accumulators so the epilogue of one unit overlaps the MMAs of
+//             the next
+//   warps 2-9 epilogue: each thread owns one batch row and 128 vocabulary
+//             columns (one output tile); it reads its logits from tensor
+//             memory, scales by 1/T, masks, adds Philox Gumbel noise, and
+//             keeps the running (max, argmax) and optionally the log-sum-exp
+//             -- or, in the top-K modes, the best 4 or 16 (score, id)
+// Only (m_t, i_t[, L_t]) -- or the top-K list -- per (row, 128-id tile)
+// leaves the chip.
+//
+// Stage 2 ("Stage 2 (Reduction)") is fused: each tile winner is folded into a
+// per-row 64-bit key with an order-free atomic max, and the last CTA to finish
+// writes the sampled ids (lowest id on ties) and clears the keys.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "fs_noise.cuh"
+#include "fs_ptx.cuh"
+#include "fs_sample.h"
+
+namespace fs {
+
+constexpr int kBlockM = 128;   // batch rows per unit = tensor-memory lanes
+constexpr int kBlockN = 256;   // vocabulary ids per unit = accumulator columns
+constexpr int kBlockK = 64;    // bf16 elements per 128-byte swizzled row
+constexpr int kUmmaK = 16;     // K of one kind::f16 MMA
+constexpr int kStages = 4;
+constexpr int kTileV = FS_TILE;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr uint32_t kSmemA = kBlockM * kBlockK * 2;  // H slice, 16 KB
+constexpr uint32_t kSmemB = kBlockN * kBlockK * 2;  // W slice, 32 KB
+constexpr uint32_t kStageBytes = kSmemA + kSmemB;
+constexpr uint32_t kTmemCols = 2 * kBlockN;         // two fp32 accumulators
+constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kBlockM, kBlockN);
+constexpr size_t kBarOffset = size_t(kStages) * kStageBytes;
+constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kBarOffset + 256;
+static_assert(kBlockN == 2 * kTileV, "one unit covers two output tiles");
+static_assert(kBlockK * 2 == 128, "one K slice row is one 128-byte swizzle row");
+
+enum : int { kErrWaitTimeout = 1 };
+
+__device__ int g_error_word = 0;
+
+struct Stage1Params {
+  int32_t B, V;
+  int32_t n_tiles;   // ceil(V / 128)
+  int32_t n_mt;      // ceil(B / 128)
+  int32_t n_kb;      // ceil(d / 64)
+  const float* temperature;
+  const uint32_t* mask;
+  int64_t mask_ld;
+  const uint64_t* seeds;
+  uint64_t seed, offset;
+  float* tile_max;             // per-tile outputs, or null
+  int32_t* tile_idx;
+  float* tile_lse;
+  int64_t* out_idx;            // sampled ids, or null (per-tile outputs only)
+  float* out_max;              // optional: the row's largest noisy score
+  int32_t vocab_offset;        // global id of W's first row (a multiple of 4)
+  unsigned long long* row_keys;  // [B] packed (score, id) maxima, zero between calls
+  uint32_t* ticket;            // CTAs finished so far, wraps back to zero
+  float* topk_score;           // top-K modes: [B, n_tiles, cap] best scores per tile
+  int32_t* topk_idx;           //              [B, n_tiles, cap] their global ids
+  uint64_t wait_limit_ns;
+  uint32_t h_box_rows;  // rows of the H box: min(128, B rounded up to 8)
+};
+
+// Bounded mbarrier waits: past the limit the CTA raises its abort flag and
+// the device error word, and every role winds down instead of spinning.
+struct Waiter {
+  volatile uint32_t* abort_flag;
+  uint64_t limit_ns;
+
+  __device__ bool wait(uint64_t* bar, uint32_t parity) const {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::global_timer_ns();
+    while (true) {
+      if (ptx::mbar_try_wait(bar, parity)) return true;
+      if (*abort_flag) return false;
+      if (ptx::global_timer_ns() - t0 > limit_ns) {
+        *abort_flag = 1u;
+        atomicOr(&g_error_word, kErrWaitTimeout);
+        return false;
+      }
+    }
+  }
+  // Used while winding down: ignores the abort flag, still bounded.
+  __device__ bool drain(uint64_t* bar, uint32_t parity) const {
+    const uint64_t t0 = ptx::global_timer_ns();
+    while (!ptx::mbar_try_wait(bar, parity)) {
+      if (ptx::global_timer_ns() - t0 > limit_ns) {
+        atomicOr(&g_error_word, kErrWaitTimeout);
+        return false;
+      }
+    }
+    return true;
+  }
+};
+
+// (score, id) as one unsigned 64-bit key whose order is: higher score first,
+// then lower id (the tie rule).  The score's bits are mapped to an order-
+// preserving unsigned word (-0 folded into +0); every valid key is nonzero.
+__device__ __forceinline__ unsigned long long pack_key(float m, int32_t idx) {
+  uint32_t b = __float_as_uint(m + 0.0f);
+  b = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return (static_cast<unsigned long long>(b) << 32) | (0xFFFFFFFFu - static_cast<uint32_t>(idx));
+}
+
+__device__ __forceinline__ int64_t unpack_idx(unsigned long long key) {
+  return key == 0ull ? int64_t(-1) : int64_t(0xFFFFFFFFu - static_cast<uint32_t>(key));
+}
+
+__device__ __forceinline__ float unpack_score(unsigned long long key) {
+  if (key == 0ull) return -INFINITY;
+  const uint32_t b = static_cast<uint32_t>(key >> 32);
+  return __uint_as_float((b & 0x80000000u) ? (b & 0x7FFFFFFFu) : ~b);
+}
+
+// One 32-column chunk of a sampling row, in base-2 units: s2 = l * (log2 e / T)
+// - log2(-log2 u), which is s * log2(e) shifted by a constant, so it has the
+// same argmax.  Updates the running maximum `best2` and, if this chunk holds
+// a new maximum, its position `best_j` in the chunk (else leaves -1).
+template <bool kMasked>
+__device__ __forceinline__ void sample_chunk(const uint32_t (&r)[32], uint32_t allow,
+                                             float scale2, uint32_t ctr0, uint32_t ctr_row,
+                                             uint32_t ctr_lo, uint32_t ctr_hi,
+                                             const PhiloxSchedule& ks, float& best2,
+                                             int& best_j) {
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    const uint4 rnd = philox4x32_10(make_uint4(ctr0 + g, ctr_row, ctr_lo, ctr_hi), ks);
+    const uint32_t words[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int j = g * 4 + i;
+      const float s2 = fmaf(__uint_as_float(r[j]), scale2, -gumbel_log2_from_word(words[i]));
+      if ((!kMasked || ((allow >> j) & 1u)) && s2 > best2) {
+        best2 = s2;
+        best_j = j;
+      }
+    }
+  }
+}
+
+template <bool kMasked>
+__device__ __forceinline__ void greedy_chunk(const uint32_t (&r)[32], uint32_t allow,
+                                             float& best, int& best_j) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const float l = __uint_as_float(r[j]);
+    if ((!kMasked || ((allow >> j) & 1u)) && l > best) {
+      best = l;
+      best_j = j;
+    }
+  }
+}
+
+// One thread, one batch row, one 128-id output tile: read the logits from
+// tensor memory 32 columns at a time and reduce them to (m_t, i_t[, L_t]).
+template <bool kWantLse>
+__device__ __forceinline__ void epilogue_tile(const Stage1Params& p, uint32_t taddr, int row,
+                                              int tile) {
+  const bool valid_row = row < p.B;
+  float T = 1.0f;
+  uint64_t seed = p.seed;
+  const uint32_t* mrow = nullptr;
+  if (valid_row) {
+    if (p.temperature) T = p.temperature[row];
+    if (p.seeds) seed = p.seeds[row];
+    if (p.mask) mrow = p.mask + int64_t(row) * p.mask_ld;
+  }
+  const bool greedy = !(T > 0.0f) || isinf(T);
+  const float scale2 = greedy ? 1.0f : kLog2e / T;  // l -> l' in base-2 units
+  const PhiloxSchedule ks(seed);
+  const uint32_t ctr_row = static_cast<uint32_t>(row);
+  const uint32_t ctr_lo = static_cast<uint32_t>(p.offset);
+  const uint32_t ctr_hi = static_cast<uint32_t>(p.offset >> 32);
+
+  float best = -INFINITY;  // greedy: max l; sampling: max s2
+  int32_t best_idx = -1;
+  float run_max = -INFINITY, run_sum = 0.0f;  // base-2 log-sum-exp state
+  const int v_tile = tile * kTileV;
+
+#pragma unroll 1
+  for (int c = 0; c < kTileV / 32; ++c) {
+    uint32_t r[32];
+    ptx::tmem_ld_32x32b_x32(taddr + uint32_t(c * 32), r);
+    ptx::tmem_wait_ld();
+    if (!valid_row) continue;
+    const int v0 = v_tile + c * 32;
+    uint32_t allow = mrow ? mrow[v0 >> 5] : 0xFFFFFFFFu;
+    const int n_in = p.V - v0;
+    if (n_in < 32) allow &= (n_in <= 0) ? 0u : ((1u << n_in) - 1u);
+    int best_j = -1;
+    if (greedy) {
+      if (allow == 0xFFFFFFFFu)
+        greedy_chunk<false>(r, allow, best, best_j);
+      else
+        greedy_chunk<true>(r, allow, best, best_j);
+    } else {
+      const uint32_t ctr0 = static_cast<uint32_t>((p.vocab_offset + v0) >> 2);
+      if (allow == 0xFFFFFFFFu)
+        sample_chunk<false>(r, allow, scale2, ctr0, ctr_row, ctr_lo, ctr_hi, ks, best, best_j);
+      else
+        sample_chunk<true>(r, allow, scale2, ctr0, ctr_row, ctr_lo, ctr_hi, ks, best, best_j);
+    }
+    if (best_j >= 0) best_idx = p.vocab_offset + v0 + best_j;
+    if (kWantLse && !greedy) {
+      float cm = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if ((allow >> j) & 1u) cm = fmaxf(cm, __uint_as_float(r[j]) * scale2);
+      if (cm > -INFINITY) {
+        const float m_new = fmaxf(run_max, cm);
+        float acc = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if ((allow >> j) & 1u) acc += ex2_approx(fmaf(__uint_as_float(r[j]), scale2, -m_new));
+        run_sum = fmaf(run_sum, ex2_approx(run_max - m_new), acc);
+        run_max = m_new;
+      }
+    }
+  }
+  if (!valid_row) return;
+  // Back to natural units: s = ln2 * (s2 - log2(ln 2)).
+  const float m = (greedy || best_idx < 0) ? best : kLn2 * (best - kLog2Ln2);
+  // Fold the tile's winner into the row's running maximum: the key orders by
+  // score, then by lower id, so the result does not depend on arrival order.
+  if (p.out_idx != nullptr && best_idx >= 0) atomicMax(p.row_keys + row, pack_key(m, best_idx));
+  if (p.tile_max == nullptr) return;
+  const int64_t o = int64_t(row) * p.n_tiles + tile;
+  p.tile_max[o] = m;
+  p.tile_idx[o] = best_idx;
+  if (kWantLse) {
+    float L = best;  // greedy rows: the largest unmasked logit
+    if (!greedy) L = run_max > -INFINITY ? (run_max + lg2_approx(run_sum)) * kLn2 : -INFINITY;
+    p.tile_lse[o] = L;
+  }
+}
+
+// Insert (s, id) into a list sorted by decreasing score whose last entry it
+// beats.  Equal scores keep their order, so with ids visited in increasing
+// order the lower id stays first (the tie rule).
+template <int KC>
+__device__ __forceinline__ void topk_insert(float (&ts)[KC], int32_t (&ti)[KC], float s,
+                                            int32_t id) {
+  ts[KC - 1] = s;
+  ti[KC - 1] = id;
+#pragma unroll
+  for (int q = KC - 1; q > 0; --q) {
+    const bool up = ts[q] > ts[q - 1];
+    const float a = ts[q], b = ts[q - 1];
+    const int32_t ia = ti[q], ib = ti[q - 1];
+    ts[q - 1] = up ? a : b;
+    ts[q] = up ? b : a;
+    ti[q - 1] = up ? ia : ib;
+    ti[q] = up ? ib : ia;
+  }
+}
+
+// Top-K form of epilogue_tile: the KC largest noisy scores of the row's tile
+// and their global ids, best first (-inf / -1 past the unmasked count),
+// written to the workspace.  By the Gumbel-top-k property the K largest scores
+// of a row are K draws without replacement from softmax(l'), in draw order.
+template <int KC>
+__device__ __forceinline__ void epilogue_tile_topk(const Stage1Params& p, uint32_t taddr,
+                                                   int row, int tile) {
+  const bool valid_row = row < p.B;
+  float T = 1.0f;
+  uint64_t seed = p.seed;
+  const uint32_t* mrow = nullptr;
+  if (valid_row) {
+    if (p.temperature) T = p.temperature[row];
+    if (p.seeds) seed = p.seeds[row];
+    if (p.mask) mrow = p.mask + int64_t(row) * p.mask_ld;
+  }
+  const bool greedy = !(T > 0.0f) || isinf(T);
+  const float scale2 = greedy ? 1.0f : kLog2e / T;
+  const PhiloxSchedule ks(seed);
+  const uint32_t ctr_row = static_cast<uint32_t>(row);
+  const uint32_t ctr_lo = static_cast<uint32_t>(p.offset);
+  const uint32_t ctr_hi = static_cast<uint32_t>(p.offset >> 32);
+  float ts[KC];
+  int32_t ti[KC];
+#pragma unroll
+  for (int q = 0; q < KC; ++q) {
+    ts[q] = -INFINITY;
+    ti[q] = -1;
+  }
+  const int v_tile = tile * kTileV;
+#pragma unroll 1
+  for (int c = 0; c < kTileV / 32; ++c) {
+    uint32_t r[32];
+    ptx::tmem_ld_32x32b_x32(taddr + uint32_t(c * 32), r);
+    ptx::tmem_wait_ld();
+    if (!valid_row) continue;
+    const int v0 = v_tile + c * 32;
+    uint32_t allow = mrow ? mrow[v0 >> 5] : 0xFFFFFFFFu;
+    const int n_in = p.V - v0;
+    if (n_in < 32) allow &= (n_in <= 0) ? 0u : ((1u << n_in) - 1u);
+    const int32_t id0 = p.vocab_offset + v0;
+    if (greedy) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float l = __uint_as_float(r[j]);
+        if (((allow >> j) & 1u) && l > ts[KC - 1]) topk_insert<KC>(ts, ti, l, id0 + j);
+      }
+      continue;
+    }
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      const uint4 rnd = philox4x32_10(
+          make_uint4(static_cast<uint32_t>(id0 >> 2) + g, ctr_row, ctr_lo, ctr_hi), ks);
+      const uint32_t words[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int j = g * 4 + i;
+        const float s2 = fmaf(__uint_as_float(r[j]), scale2, -gumbel_log2_from_word(words[i]));
+        if (((allow >> j) & 1u) && s2 > ts[KC - 1]) topk_insert<KC>(ts, ti, s2, id0 + j);
+      }
+    }
+  }
+  if (!valid_row) return;
+  const int64_t o = (int64_t(row) * p.n_tiles + tile) * KC;
+#pragma unroll
+  for (int q = 0; q < KC; ++q) {
+    const float m = (greedy || ti[q] < 0) ? ts[q] : kLn2 * (ts[q] - kLog2Ln2);
+    p.topk_score[o + q] = m;
+    p.topk_idx[o + q] = ti[q];
+  }
+}
+
+// Stage 2 ("Stage 2 (Reduction)"), fused: the last CTA to finish turns the
+// per-row maxima into sampled ids and clears them for the next call.  The
+// ticket wraps to zero on the last arrival, so it too is left cleared.  Called
+// by every thread of every CTA once its work is done (and its row-key updates
+// fenced).
+__device__ __forceinline__ void finish_rows(const Stage1Params& p) {
+  if (p.out_idx == nullptr) return;
+  __shared__ uint32_t s_is_last;
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_is_last = (atomicInc(p.ticket, gridDim.x - 1u) == gridDim.x - 1u) ? 1u : 0u;
+  }
+  __syncthreads();
+  if (s_is_last) {
+    __threadfence();
+    for (int r = threadIdx.x; r < p.B; r += blockDim.x) {
+      const unsigned long long key = atomicExch(p.row_keys + r, 0ull);
+      p.out_idx[r] = unpack_idx(key);
+      if (p.out_max != nullptr) p.out_max[r] = unpack_score(key);
+    }
+  }
+}
+
+// Epilogue modes (a template parameter of both stage-1 kernels).
+enum : int {
+  kModeSample = 0,  // (m_t, i_t) per tile, row maxima
+  kModeLse = 1,     // ... plus the tile log-sum-exp
+  kModeTop4 = 2,    // the 4 best (score, id) per tile, for K <= 4 draws without replacement
+  kModeTop16 = 3,   // the 16 best, for K <= 16
+};
+__host__ __device__ constexpr int topk_cap(int mode) {
+  return mode == kModeTop4 ? 4 : mode == kModeTop16 ? 16 : 1;
+}
+
+template <int kMode>
+__device__ __forceinline__ void epilogue_unit(const Stage1Params& p, uint32_t taddr, int row,
+                                              int tile) {
+  if constexpr (kMode == kModeSample || kMode == kModeLse)
+    epilogue_tile<kMode == kModeLse>(p, taddr, row, tile);
+  else
+    epilogue_tile_topk<topk_cap(kMode)>(p, taddr, row, tile);
+}
+
+// Single-CTA stage 1: a unit is (vocabulary block vt of 256 ids, batch block mt
+// of 128 rows), computed by one CTA with M = 128, N = 256 MMAs; units are
+// ordered vocabulary-major so the batch blocks of one vocabulary block run on
+// neighbouring CTAs at the same time and the second read of W hits L2.
+template <int kMode>
+__global__ void __launch_bounds__(kThreads, 1)
+    stage1_kernel(const __grid_constant__ CUtensorMap tmap_h,
+                  const __grid_constant__ CUtensorMap tmap_w, const Stage1Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kBarOffset);
+  uint64_t* empty_bar = full_bar + kStages;
+  uint64_t* tfull_bar = empty_bar + kStages;
+  uint64_t* tempty_bar = tfull_bar + 2;
+  uint64_t* drain_bar = tempty_bar + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  volatile uint32_t* abort_flag = tmem_holder + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n_units = ((p.V + kBlockN - 1) / kBlockN) * p.n_mt;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(&full_bar[s], 1);
+      ptx::mbar_init(&empty_bar[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&tfull_bar[a], 1);
+      ptx::mbar_init(&tempty_bar[a], kEpiWarps);
+    }
+    ptx::mbar_init(drain_bar, 1);
+    *abort_flag = 0u;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tmap_h);
+    ptx::prefetch_tmap(&tmap_w);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_holder, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const Waiter waiter{abort_flag, p.wait_limit_ns};
+
+  if (warp == 0) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      const uint64_t pol_w = p.n_mt > 1 ? ptx::policy_evict_normal() : ptx::policy_evict_first();
+      const uint64_t pol_h = ptx::policy_evict_last();
+      uint32_t stage = 0, phase = 0, issued = 0;
+      bool ok = true;
+      for (int unit = blockIdx.x; ok && unit < n_units; unit += gridDim.x) {
+        const int vt = unit / p.n_mt, mt = unit % p.n_mt;
+        // Each vocabulary block starts its K loop at its own slice, so CTAs
+        // working at the same moment read different H lines.  The start
+        // depends on the (global) vocabulary block only, so a row's sums (and
+        // its sample) do not depend on the batch size or on the sharding.
+        const int k_start =
+            int((uint32_t(vt + (p.vocab_offset >> 8)) * 5u) % uint32_t(p.n_kb));
+        for (int kk = 0; kk < p.n_kb; ++kk) {
+          const int kb = kk + k_start < p.n_kb ? kk + k_start : kk + k_start - p.n_kb;
+          if (!waiter.wait(&empty_bar[stage], phase ^ 1u)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + size_t(stage) * kStageBytes;
+          ptx::mbar_arrive_expect_tx(&full_bar[stage], kSmemB + p.h_box_rows * 128u);
+          ptx::tma_load_2d(sa + kSmemA, &tmap_w, &full_bar[stage], kb * kBlockK, vt * kBlockN,
+                           pol_w);
+          ptx::tma_load_2d(sa, &tmap_h, &full_bar[stage], kb * kBlockK, mt * kBlockM, pol_h);
+          ++issued;
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // Every issued copy must land before the CTA (and its shared memory)
+      // goes away: wait for the last fill of each stage.
+      for (uint32_t s = 0; s < uint32_t(kStages); ++s) {
+        const uint32_t fills = issued / kStages + (s < issued % kStages ? 1u : 0u);
+        if (fills) waiter.drain(&full_bar[s], (fills - 1u) & 1u);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int unit = blockIdx.x; ok && unit < n_units; unit += gridDim.x) {
+        if (!waiter.wait(&tempty_bar[acc], acc_phase ^ 1u)) break;
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * kBlockN;
+        for (int kb = 0; kb < p.n_kb; ++kb) {
+          if (!waiter.wait(&full_bar[stage], phase)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t sa = ptx::smem_u32(smem + size_t(stage) * kStageBytes);
+          const uint32_t sb = sa + kSmemA;
+#pragma unroll
+          for (int k = 0; k < kBlockK / kUmmaK; ++k) {
+            ptx::mma_bf16(d_tmem, ptx::smem_desc_sw128(sa + k * kUmmaK * 2),
+                          ptx::smem_desc_sw128(sb + k * kUmmaK * 2), kIdesc,
+                          (kb | k) != 0 ? 1u : 0u);
+          }
+          ptx::mma_commit(&empty_bar[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit(&tfull_bar[acc]);
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      // All MMAs must be complete before tensor memory is released.
+      ptx::mma_commit(drain_bar);
+      waiter.drain(drain_bar, 0);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue ----------------
+    const int e = warp - 2;
+    const int quad = warp & 3;  // the tensor-memory lane quadrant this warp may read
+    const int half = e >> 2;    // which 128-column half of the unit
+    uint32_t acc = 0, acc_phase = 0;
+    for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
+      const int vt = unit / p.n_mt, mt = unit % p.n_mt;
+      int ok = 0;
+      if (lane == 0) ok = waiter.wait(&tfull_bar[acc], acc_phase) ? 1 : 0;
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const int row0 = mt * kBlockM + quad * 32;
+      const int tile = vt * 2 + half;
+      if (row0 < p.B && tile < p.n_tiles) {
+        const uint32_t taddr =
+            tmem_base + (uint32_t(quad * 32) << 16) + acc * kBlockN + uint32_t(half * kTileV);
+        epilogue_unit<kMode>(p, taddr, row0 + lane, tile);
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&tempty_bar[acc]);
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  ptx::tc_fence_before();
+  __threadfence();  // this thread's row-key updates are visible device-wide
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem_base, kTmemCols);
+  }
+  finish_rows(p);
+}
+
+// ---------------------------------------------------------------------------
+// Stage 1 for batches of more than 128 rows: CTA pairs (2-CTA clusters) run
+// M = 256, N = 256, K = 16 MMAs (cta_group::2).  A unit is (vocabulary block vt
+// of 256 ids, pair block mp of 256 batch rows).  CTA r of the pair loads batch
+// rows mp*256 + r*128 .. +127 (its half of A) and vocabulary rows vt*256 +
+// r*128 .. +127 (its half of B) into its own shared memory, 32 KB a stage, so
+// six stages fit; every copy signals the even ("leader") CTA's full barrier.
+// The leader's single MMA thread accumulates into both CTAs' tensor memory
+// (rows r*128.. in CTA r, all 256 columns) and multicasts its commits to both
+// CTAs' barriers.  Each CTA's epilogue reads its own 128 rows; the leader's
+// "tensor memory empty" barrier collects the epilogue warps of both CTAs.
+constexpr int kPairStages = 6;
+constexpr uint32_t kPairSmemA = 128 * kBlockK * 2;  // 16 KB: this CTA's batch rows
+constexpr uint32_t kPairSmemB = 128 * kBlockK * 2;  // 16 KB: this CTA's vocabulary rows
+constexpr uint32_t kPairStageBytes = kPairSmemA + kPairSmemB;
+constexpr size_t kPairBarOffset = size_t(kPairStages) * kPairStageBytes;
+constexpr size_t kPairSmemBytes = 1024 + kPairBarOffset + 256;
+constexpr uint32_t kPairIdesc = ptx::idesc_bf16_f32(2 * kBlockM, kBlockN);
+static_assert(kPairSmemBytes <= 232448, "pair kernel shared memory");
+
+template <int kMode>
+__global__ void __launch_bounds__(kThreads, 1)
+    stage1_pair_kernel(const __grid_constant__ CUtensorMap tmap_h,
+                       const __grid_constant__ CUtensorMap tmap_w, const Stage1Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kPairBarOffset);
+  uint64_t* empty_bar = full_bar + kPairStages;
+  uint64_t* tfull_bar = empty_bar + kPairStages;
+  uint64_t* tempty_bar = tfull_bar + 2;
+  uint64_t* drain_bar = tempty_bar + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  volatile uint32_t* abort_flag = tmem_holder + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int rank = int(ptx::cluster_ctarank());
+  const bool leader = rank == 0;
+  const int pair_id = int(blockIdx.x) >> 1;
+  const int n_pairs = int(gridDim.x) >> 1;
+  const int n_mp = (p.B + 2 * kBlockM - 1) / (2 * kBlockM);
+  const int n_units = ((p.V + kBlockN - 1) / kBlockN) * n_mp;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPairStages; ++s) {
+      ptx::mbar_init(&full_bar[s], 1);
+      ptx::mbar_init(&empty_bar[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&tfull_bar[a], 1);
+      ptx::mbar_init(&tempty_bar[a], 2 * kEpiWarps);
+    }
+    ptx::mbar_init(drain_bar, 1);
+    *abort_flag = 0u;
+    ptx::fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tmap_h);
+    ptx::prefetch_tmap(&tmap_w);
+  }
+  if (warp == 1) {  // one warp in each CTA of the pair, together
+    ptx::tmem_alloc_pair(tmem_holder, kTmemCols);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::cluster_sync();  // both CTAs' barriers exist before either uses the other's
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const Waiter waiter{abort_flag, p.wait_limit_ns};
+
+  if (warp == 0) {
+    // ---------------- TMA producer (both CTAs) ----------------
+    if (lane == 0) {
+      const uint64_t pol_w = n_mp > 1 ? ptx::policy_evict_normal() : ptx::policy_evict_first();
+      const uint64_t pol_h = ptx::policy_evict_last();
+      uint32_t stage = 0, phase = 0, issued = 0;
+      bool ok = true;
+      for (int u = pair_id; ok && u < n_units; u += n_pairs) {
+        const int vt = u / n_mp, mp = u % n_mp;
+        const int k_start =
+            int((uint32_t(vt + (p.vocab_offset >> 8)) * 5u) % uint32_t(p.n_kb));
+        // Rows past the end are read from the last valid row instead (their
+        // accumulator rows / columns are never used), so no box lies wholly
+        // outside its tensor.
+        const int a_y = min(mp * 2 * kBlockM + rank * kBlockM, p.B - 1);
+        const int w_y = min(vt * kBlockN + rank * (kBlockN / 2), p.V - 1);
+        for (int kk = 0; kk < p.n_kb; ++kk) {
+          const int kb = kk + k_start < p.n_kb ? kk + k_start : kk + k_start - p.n_kb;
+          if (!waiter.wait(&empty_bar[stage], phase ^ 1u)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + size_t(stage) * kPairStageBytes;
+          const uint32_t full_addr = ptx::cluster_addr(&full_bar[stage], 0);
+          if (leader) ptx::mbar_arrive_expect_tx(&full_bar[stage], 2 * kPairStageBytes);
+          ptx::tma_load_2d_pair(sa + kPairSmemA, &tmap_w, full_addr, kb * kBlockK, w_y, pol_w);
+          ptx::tma_load_2d_pair(sa, &tmap_h, full_addr, kb * kBlockK, a_y, pol_h);
+          ++issued;
+          if (++stage == kPairStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // The leader's full barriers see both CTAs' copies land; wait for the
+      // last fill of each stage before anything goes away.
+      if (leader) {
+        for (uint32_t s = 0; s < uint32_t(kPairStages); ++s) {
+          const uint32_t fills = issued / kPairStages + (s < issued % kPairStages ? 1u : 0u);
+          if (fills) waiter.drain(&full_bar[s], (fills - 1u) & 1u);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------- MMA issuer (leader CTA only) ----------------
+    if (lane == 0 && leader) {
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int u = pair_id; ok && u < n_units; u += n_pairs) {
+        if (!waiter.wait(&tempty_bar[acc], acc_phase ^ 1u)) break;
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * kBlockN;
+        for (int kb = 0; kb < p.n_kb; ++kb) {
+          if (!waiter.wait(&full_bar[stage], phase)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t sa = ptx::smem_u32(smem + size_t(stage) * kPairStageBytes);
+          const uint32_t sb = sa + kPairSmemA;
+#pragma unroll
+          for (int k = 0; k < kBlockK / kUmmaK; ++k) {
+            ptx::mma_bf16_pair(d_tmem, ptx::smem_desc_sw128(sa + k * kUmmaK * 2),
+                               ptx::smem_desc_sw128(sb + k * kUmmaK * 2), kPairIdesc,
+                               (kb | k) != 0 ? 1u : 0u);
+          }
+          ptx::mma_commit_pair_multicast(&empty_bar[stage], 0x3);
+          if (++stage == kPairStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit_pair_multicast(&tfull_bar[acc], 0x3);
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      ptx::mma_commit_pair(drain_bar);
+      waiter.drain(drain_bar, 0);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- epilogue (both CTAs) ----------------
+    const int e = warp - 2;
+    const int quad = warp & 3;
+    const int half = e >> 2;
+    const uint32_t tempty_addr0 = ptx::cluster_addr(&tempty_bar[0], 0);
+    const uint32_t tempty_addr1 = ptx::cluster_addr(&tempty_bar[1], 0);
+    uint32_t acc = 0, acc_phase = 0;
+    for (int u = pair_id; u < n_units; u += n_pairs) {
+      const int vt = u / n_mp, mp = u % n_mp;
+      int ok = 0;
+      if (lane == 0) ok = waiter.wait(&tfull_bar[acc], acc_phase) ? 1 : 0;
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const int row0 = mp * 2 * kBlockM + rank * kBlockM + quad * 32;
+      const int tile = vt * 2 + half;
+      if (row0 < p.B && tile < p.n_tiles) {
+        const uint32_t taddr =
+            tmem_base + (uint32_t(quad * 32) << 16) + acc * kBlockN + uint32_t(half * kTileV);
+        epilogue_unit<kMode>(p, taddr, row0 + lane, tile);
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive_cluster(acc == 0 ? tempty_addr0 : tempty_addr1);
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  ptx::tc_fence_before();
+  __threadfence();
+  __syncthreads();
+  // Both CTAs are done with each other's barriers and the leader's MMAs have
+  // drained before the pair's tensor memory is released.
+  ptx::cluster_sync();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+  ptx::cluster_sync();
+  finish_rows(p);
+}
+
+// Diagnostic: the bounded wait of the sampling kernels, on an mbarrier that no
+// thread ever arrives on.  It gives up after limit_ns, records the timeout in
+// the device error word, and returns -- the path a stalled pipeline takes.
+__global__ void wait_timeout_kernel(uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ uint32_t abort_word;
+  ptx::mbar_init(&bar, 1);
+  abort_word = 0u;
+  ptx::fence_barrier_init();
+  const Waiter waiter{&abort_word, limit_ns};
+  waiter.wait(&bar, 0);  // phase 0 never completes
+}
+
+// The noise stage 1 adds, element by element (diagnostic entry point).
+__global__ void noise_kernel(const uint64_t* __restrict__ seeds, uint64_t seed, uint64_t offset,
+                             int64_t b0, int64_t nb, int64_t v0, int64_t nv,
+                             float* __restrict__ out) {
+  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= nb * nv) return;
+  const int64_t b = b0 + i / nv, v = v0 + i % nv;
+  const uint64_t sd = seeds ? seeds[b] : seed;
+  const uint4 r = philox4x32_10(
+      make_uint4(static_cast<uint32_t>(v >> 2), static_cast<uint32_t>(b),
+                 static_cast<uint32_t>(offset), static_cast<uint32_t>(offset >> 32)),
+      PhiloxSchedule(sd));
+  out[i] = gumbel_from_word(select_word(r, static_cast<uint32_t>(v & 3)));
+}
+
+}  // namespace fs
