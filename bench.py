@@ -60,13 +60,15 @@ def load_peaks():
     return dict(FALLBACK_PEAKS, source="fallback")
 
 
-def algorithmic(B, d, V, *, mask=False, seeds=True, temperature=True):
+def algorithmic(B, d, V, *, mask=False, seeds=True, temperature=True, tiles=False):
     """Bytes and flops one sampling call must move / do: W and H once, the
-    per-row parameters and mask bits, and the sampled ids (int64)."""
+    per-row parameters and mask bits, the sampled ids (int64) and, with
+    ``tiles``, the per-(row, 128-id tile) max, argmax and log-mass (4 B each)."""
     by = V * d * 2 + B * d * 2 + B * 8
     by += B * 4 if temperature else 0
     by += B * 8 if seeds else 0
     by += B * ((V + 31) // 32) * 4 if mask else 0
+    by += B * ((V + 127) // 128) * 12 if tiles else 0
     return by, 2.0 * B * V * d
 
 
@@ -254,11 +256,12 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     out = torch.empty(B, dtype=torch.int64, device=dev)
     ws = torch.zeros(fs.fs_workspace_size(B, V), dtype=torch.uint8, device=dev)
+    tiles = tile_outputs(w, B, dev)
 
     def call(k, base=0):
         fs.fs_sample(inp["H"], inp["W"], temperature=inp["temperature"], seeds=inp["seeds"],
                      vocab_mask=inp["vocab_mask"], offset=base + k, out_idx=out, workspace=ws,
-                     stream=stream)
+                     stream=stream, **tiles)
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -280,23 +283,25 @@ def run_ours(args):
             _, inp2 = make_inputs_like(w, b2, dev, inp["W"])
             o2 = torch.empty(b2, dtype=torch.int64, device=dev)
             ws2 = torch.zeros(fs.fs_workspace_size(b2, V), dtype=torch.uint8, device=dev)
+            t2 = tile_outputs(w, b2, dev)
 
             def c2(k):
                 fs.fs_sample(inp2["H"], inp2["W"], temperature=inp2["temperature"],
-                             seeds=inp2["seeds"], offset=k, out_idx=o2, workspace=ws2,
-                             stream=stream)
+                             seeds=inp2["seeds"], vocab_mask=inp2["vocab_mask"], offset=k,
+                             out_idx=o2, workspace=ws2, stream=stream, **t2)
 
             for k in range(5):
                 c2(k)
             torch.cuda.synchronize()
             ts0 = time.time()
             us2 = time_calls(c2, args.sweep_steps, stream) * 1000.0 / args.sweep_steps
-            rf = roofline(b2, d, V, us2, peaks, seeds=inp2["seeds"] is not None)
+            rf = roofline(b2, d, V, us2, peaks, seeds=inp2["seeds"] is not None,
+                          mask=inp2["vocab_mask"] is not None, tiles=bool(t2))
             sweep.append({"B": b2, "us_per_call": round(us2, 2),
                           "tokens_per_s": round(b2 / (us2 * 1e-6), 1), "bound": rf["bound"],
                           "achieved": rf["achieved"], "unit": rf["unit"], "frac": rf["frac"],
                           "window": (ts0, time.time())})
-            del inp2, o2, ws2
+            del inp2, o2, ws2, t2
     # The K-draws-without-replacement mode on the same batch (an extension of
     # the headline path; reported beside it, not in it).
     extensions = {}
@@ -307,7 +312,8 @@ def run_ours(args):
 
             def ctk(k, K=K, tk_out=tk_out, tk_ws=tk_ws):
                 fs.fs_sample_topk(inp["H"], inp["W"], K, temperature=inp["temperature"],
-                                  seeds=inp["seeds"], offset=k, out_topk_idx=tk_out,
+                                  seeds=inp["seeds"], vocab_mask=inp["vocab_mask"],
+                                  offset=k, out_topk_idx=tk_out,
                                   workspace=tk_ws, stream=stream)
 
             for k in range(3):
@@ -316,8 +322,8 @@ def run_ours(args):
             extensions[f"topk{K}_us_per_call"] = round(us_tk, 2)
             del tk_out, tk_ws
 
-    # End to end through the C ABI: each step's inputs (H, temperatures, seeds)
-    # go host -> device in one copy from one pinned buffer, fs_sample runs from
+    # End to end through the C ABI: each step's inputs (H, temperatures, seeds,
+    # mask) go host -> device in one copy from one pinned buffer, fs_sample runs from
     # an argument block built once (only the offset changes), and the sampled
     # ids come back device -> host before the next step starts.
     import ctypes
@@ -326,6 +332,8 @@ def run_ours(args):
              inp["temperature"].contiguous().view(torch.uint8).view(-1)]
     if inp["seeds"] is not None:
         parts.append(inp["seeds"].contiguous().view(torch.uint8).view(-1))
+    if inp["vocab_mask"] is not None:
+        parts.append(inp["vocab_mask"].contiguous().view(torch.uint8).view(-1))
     sizes = [t.numel() for t in parts]
     pad = [(-n) % 256 for n in sizes]  # keep each input 256-byte aligned
     host_in = torch.empty(sum(sizes) + sum(pad), dtype=torch.uint8).pin_memory()
@@ -337,15 +345,19 @@ def run_ours(args):
         pos += n + q
     Hd = views[0].view(torch.bfloat16).view(B, d)
     Td = views[1].view(torch.float32)
-    Sd = views[2].view(torch.int64) if len(views) > 2 else None
+    Sd = views[2].view(torch.int64) if inp["seeds"] is not None else None
+    Md = views[-1].view(torch.int32).view(B, -1) if inp["vocab_mask"] is not None else None
     out_h = torch.empty(B, dtype=torch.int64).pin_memory()
     args_c = fs.FsSampleArgs(
         H=Hd.data_ptr(), W=inp["W"].data_ptr(), temperature=Td.data_ptr(),
-        vocab_mask=None if inp["vocab_mask"] is None else inp["vocab_mask"].data_ptr(),
-        mask_ld=0 if inp["vocab_mask"] is None else inp["vocab_mask"].stride(0),
+        vocab_mask=None if Md is None else Md.data_ptr(),
+        mask_ld=0 if Md is None else Md.stride(0),
         seeds=None if Sd is None else Sd.data_ptr(), seed=0, offset=0, B=B, d=d, V=V,
         ldh=d, ldw=inp["W"].stride(0), out_idx=out.data_ptr(), workspace=ws.data_ptr(),
-        workspace_bytes=ws.numel())
+        workspace_bytes=ws.numel(),
+        out_tile_max=tiles["out_tile_max"].data_ptr() if tiles else None,
+        out_tile_idx=tiles["out_tile_idx"].data_ptr() if tiles else None,
+        out_tile_lse=tiles["out_tile_lse"].data_ptr() if tiles else None)
     args_ref = ctypes.byref(args_c)
     sh = ctypes.c_void_p(stream.cuda_stream)
 
@@ -375,7 +387,8 @@ def run_ours(args):
         raise SystemExit(f"device error word {code} after the benchmark")
 
     rf = roofline(B, d, V, us_call, peaks, traffic=measured_traffic(args.workload, B),
-                  seeds=inp["seeds"] is not None, mask=inp["vocab_mask"] is not None)
+                  seeds=inp["seeds"] is not None, mask=inp["vocab_mask"] is not None,
+                  tiles=bool(tiles))
     rf["kernel"] = "fs::stage1_kernel (the whole call: stage 2 is fused into it)"
     rf["duration_us"] = round(us_call, 3)
 
@@ -393,8 +406,7 @@ def run_ours(args):
         "dtype": "bf16",
         "data": "synthetic",
         "config": {
-            "workload": f"{w.name} head: d={d} V={V} B={B}, bf16 H~N(0,1) W~N(0,(2/sqrt d)^2), "
-                        "per-row T~U[0.5,1.5] with 10% greedy, per-row seeds, offset=step",
+            "workload": describe(w, B),
             "B": B, "d": d, "V": V, "global_batch": B * world,
             "l2": "inputs exceed L2 (W is %.2f GB), no flush" % (V * d * 2 / 1e9),
             "parallelism": "replicas" if world > 1 else "single-gpu",
@@ -422,7 +434,37 @@ def make_inputs_like(w, B, device, W):
     H = wl.make_hidden(B, w.d, seed=2000 + B, device=device)
     T = wl.make_temperature(w, B, seed=3000 + B, device=device)
     seeds = wl.make_seeds(B, base=4000 + B, device=device) if w.per_row_seeds else None
-    return w, {"H": H, "W": W, "temperature": T, "seeds": seeds, "vocab_mask": None}
+    mask = wl.make_mask(B, w.V, w.mask_frac, seed=5000 + B, device=device) if w.mask_frac else None
+    return w, {"H": H, "W": W, "temperature": T, "seeds": seeds, "vocab_mask": mask}
+
+
+def tile_outputs(w, B, device):
+    """Per-tile output buffers for workloads that ask for the tile log-mass."""
+    import torch
+    if not w.want_lse:
+        return {}
+    nt = (w.V + 127) // 128
+    return {"out_tile_max": torch.empty((B, nt), dtype=torch.float32, device=device),
+            "out_tile_idx": torch.empty((B, nt), dtype=torch.int32, device=device),
+            "out_tile_lse": torch.empty((B, nt), dtype=torch.float32, device=device)}
+
+
+def describe(w, B):
+    """The workload in words, from its definition."""
+    if w.temperature == "row-uniform":
+        t = "per-row T~U[0.5,1.5] with 10% greedy"
+    else:
+        t = f"T={w.t_value:g}"
+    parts = [f"{w.name} head: d={w.d} V={w.V} B={B}", "bf16 H~N(0,1) W~N(0,(2/sqrt d)^2)", t]
+    if w.outlier_frac:
+        parts.append(f"{100 * w.outlier_frac:g}% of W rows x4")
+    if w.mask_frac:
+        parts.append(f"per-row vocab mask ({100 * w.mask_frac:g}% of ids masked)")
+    parts.append("per-row seeds" if w.per_row_seeds else "one seed")
+    if w.want_lse:
+        parts.append("tile max/argmax/LSE written")
+    parts.append("offset=step")
+    return ", ".join(parts)
 
 
 def oracle_inputs(inp):
@@ -498,7 +540,7 @@ def run_reference(args):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(statistics.mean(times) * 1000.0, 3), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{w.name} head: d={d} V={V} B={B} (CPU oracle)", "B": B, "d": d,
+        "config": {"workload": describe(w, B), "B": B, "d": d,
                    "V": V, "global_batch": B, "parallelism": "cpu"},
         "cpu_baseline": {"value": round(us, 1), "unit": "us/call", "cores": o.num_threads(),
                          "kind": "oracle", "sample": sample},
