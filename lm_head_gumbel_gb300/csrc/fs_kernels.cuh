@@ -12,8 +12,8 @@
 // number of batch blocks, CTA pairs compute 256 x 256 units with cta_group::2
 // MMAs (stage1_pair_kernel below).  Single-CTA roles:
 //   warp 0    TMA producer: streams 64-wide K slices of W (256 x 64) and
-//             H (up to 128 x 64) into a 4-stage shared-memory ring (128-byte
-//             swizzle)
+//             H (up to 128 x 64) into a shared-memory ring of 4-6 stages
+//             (128-byte swizzle; the fewer H rows, the more stages)
 //   warp 1    tcgen05 MMA issuer: M=128, N=256, K=16 bf16 MMAs accumulate the
 //             unit's logits in tensor memory (fp32, 256 columns); two
 //             accumulators so the epilogue of one unit overlaps the MMAs of
@@ -47,16 +47,16 @@ constexpr int kBlockM = 128;   // batch rows per unit = tensor-memory lanes
 constexpr int kBlockN = 256;   // vocabulary ids per unit = accumulator columns
 constexpr int kBlockK = 64;    // bf16 elements per 128-byte swizzled row
 constexpr int kUmmaK = 16;     // K of one kind::f16 MMA
-constexpr int kStages = 4;
+constexpr int kMaxStages = 6;  // ring depth: as many stages as fit kRingBytes, at most 6
 constexpr int kTileV = FS_TILE;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 32 * (2 + kEpiWarps);
-constexpr uint32_t kSmemA = kBlockM * kBlockK * 2;  // H slice, 16 KB
+constexpr uint32_t kSmemA = kBlockM * kBlockK * 2;  // H slice of 128 rows, 16 KB
 constexpr uint32_t kSmemB = kBlockN * kBlockK * 2;  // W slice, 32 KB
-constexpr uint32_t kStageBytes = kSmemA + kSmemB;
+constexpr uint32_t kRingBytes = 200 * 1024;         // stages of H rows + W slice
 constexpr uint32_t kTmemCols = 2 * kBlockN;         // two fp32 accumulators
 constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kBlockM, kBlockN);
-constexpr size_t kBarOffset = size_t(kStages) * kStageBytes;
+constexpr size_t kBarOffset = kRingBytes;
 constexpr size_t kSmemBytes = 1024 /* alignment slack */ + kBarOffset + 256;
 static_assert(kBlockN == 2 * kTileV, "one unit covers two output tiles");
 static_assert(kBlockK * 2 == 128, "one K slice row is one 128-byte swizzle row");
@@ -87,6 +87,11 @@ struct Stage1Params {
   int32_t* topk_idx;           //              [B, n_tiles, cap] their global ids
   uint64_t wait_limit_ns;
   uint32_t h_box_rows;  // rows of the H box: min(128, B rounded up to 8)
+  // Single-CTA ring: a stage is the H box (h_box_rows x 128 bytes, whole
+  // 1 KB swizzle atoms) followed by the W slice; small batches get more
+  // stages, so more of W is in flight.
+  uint32_t n_stages;
+  uint32_t stage_bytes;
 };
 
 // Bounded mbarrier waits: past the limit the CTA raises its abort flag and
@@ -409,8 +414,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + kBarOffset);
-  uint64_t* empty_bar = full_bar + kStages;
-  uint64_t* tfull_bar = empty_bar + kStages;
+  uint64_t* empty_bar = full_bar + kMaxStages;
+  uint64_t* tfull_bar = empty_bar + kMaxStages;
   uint64_t* tempty_bar = tfull_bar + 2;
   uint64_t* drain_bar = tempty_bar + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain_bar + 1);
@@ -421,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_units = ((p.V + kBlockN - 1) / kBlockN) * p.n_mt;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (uint32_t s = 0; s < p.n_stages; ++s) {
       ptx::mbar_init(&full_bar[s], 1);
       ptx::mbar_init(&empty_bar[s], 1);
     }
@@ -446,6 +451,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   const Waiter waiter{abort_flag, p.wait_limit_ns};
+  const uint32_t h_bytes = p.h_box_rows * 128u;  // the H box; the W slice follows it
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -468,13 +474,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          uint8_t* sa = smem + size_t(stage) * kStageBytes;
-          ptx::mbar_arrive_expect_tx(&full_bar[stage], kSmemB + p.h_box_rows * 128u);
-          ptx::tma_load_2d(sa + kSmemA, &tmap_w, &full_bar[stage], kb * kBlockK, vt * kBlockN,
+          uint8_t* sa = smem + size_t(stage) * p.stage_bytes;
+          ptx::mbar_arrive_expect_tx(&full_bar[stage], h_bytes + kSmemB);
+          ptx::tma_load_2d(sa + h_bytes, &tmap_w, &full_bar[stage], kb * kBlockK, vt * kBlockN,
                            pol_w);
           ptx::tma_load_2d(sa, &tmap_h, &full_bar[stage], kb * kBlockK, mt * kBlockM, pol_h);
           ++issued;
-          if (++stage == kStages) {
+          if (++stage == p.n_stages) {
             stage = 0;
             phase ^= 1u;
           }
@@ -482,8 +488,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // Every issued copy must land before the CTA (and its shared memory)
       // goes away: wait for the last fill of each stage.
-      for (uint32_t s = 0; s < uint32_t(kStages); ++s) {
-        const uint32_t fills = issued / kStages + (s < issued % kStages ? 1u : 0u);
+      for (uint32_t s = 0; s < p.n_stages; ++s) {
+        const uint32_t fills = issued / p.n_stages + (s < issued % p.n_stages ? 1u : 0u);
         if (fills) waiter.drain(&full_bar[s], (fills - 1u) & 1u);
       }
     }
@@ -503,8 +509,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t sa = ptx::smem_u32(smem + size_t(stage) * kStageBytes);
-          const uint32_t sb = sa + kSmemA;
+          // A spans 128 rows; those past the H box read whatever follows it
+          // in shared memory and feed only accumulator rows that are never read.
+          const uint32_t sa = ptx::smem_u32(smem + size_t(stage) * p.stage_bytes);
+          const uint32_t sb = sa + h_bytes;
 #pragma unroll
           for (int k = 0; k < kBlockK / kUmmaK; ++k) {
             ptx::mma_bf16(d_tmem, ptx::smem_desc_sw128(sa + k * kUmmaK * 2),
@@ -512,7 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                           (kb | k) != 0 ? 1u : 0u);
           }
           ptx::mma_commit(&empty_bar[stage]);
-          if (++stage == kStages) {
+          if (++stage == p.n_stages) {
             stage = 0;
             phase ^= 1u;
           }

@@ -240,9 +240,9 @@ fs_status run_stage1(const fs_sample_args* a, int mode, Stage1Params& p, cudaStr
   const uint32_t h_rows = B >= kBlockM ? uint32_t(kBlockM) : uint32_t((B + 7) / 8 * 8);
   const int n_mt = int((B + kBlockM - 1) / kBlockM);
   // An even number of 128-row batch blocks: CTA pairs with M = 256 MMAs, each
-  // CTA holding half of the W slice (six 32 KB stages).  Otherwise single CTAs
-  // with M = 128 and the whole slice (four 48 KB stages); with an odd number of
-  // batch blocks above one, pairs would leave half a pair idle.
+  // CTA holding half of the W slice (six 32 KB stages).  Otherwise single
+  // CTAs with M = 128 and the whole slice (4-6 stages of H box + 32 KB); with
+  // an odd number of batch blocks above one, pairs would leave half a pair idle.
   const bool pair = n_mt > 1 && n_mt % 2 == 0;
   CUtensorMap tmap_h, tmap_w;
   if (!encode_2d(&tmap_h, a->H, uint64_t(d), uint64_t(B), uint64_t(a->ldh) * 2u, kBlockK,
@@ -264,6 +264,9 @@ fs_status run_stage1(const fs_sample_args* a, int mode, Stage1Params& p, cudaStr
   p.vocab_offset = int32_t(a->vocab_offset);
   p.wait_limit_ns = kWaitLimitNs;
   p.h_box_rows = h_rows;
+  p.stage_bytes = h_rows * 128u + kSmemB;  // h_rows is a multiple of 8: 1 KB swizzle atoms
+  p.n_stages = kRingBytes / p.stage_bytes < uint32_t(kMaxStages) ? kRingBytes / p.stage_bytes
+                                                                : uint32_t(kMaxStages);
   const DeviceState& ds = *g_last_state;
   switch (mode) {
     case kModeSample: return launch_mode<kModeSample>(pair, tmap_h, tmap_w, p, ds, stream);

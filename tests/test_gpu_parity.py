@@ -115,6 +115,25 @@ def test_deterministic_across_calls_and_streams():
     assert not np.array_equal(a["idx"], d["idx"])
 
 
+@pytest.mark.parametrize("V", [40000, 151936])
+def test_rows_do_not_depend_on_the_batch(V):
+    """A row's tile outputs and sample are bit-identical whatever batch it sits
+    in: B = 64 (one batch block: balanced runs of tiles, 128-id units where a
+    run cuts a vocabulary block), B = 384 (three batch blocks: single CTAs,
+    256-id units) and B = 256 (CTA pairs).  Every tile keeps its vocabulary
+    block's K order, so only the MMA shape differs."""
+    big = make_problem(384, 512, V, T="row-uniform", per_row_seeds=True, seed=12)
+    runs = {}
+    for B in (64, 256, 384):
+        sub = {k: (None if t is None else t[:B].contiguous()) if k != "W" else t
+               for k, t in big.items()}
+        runs[B] = run_device(sub, seed=5, offset=6)
+    for B in (256, 384):
+        for k in ("idx", "tile_max", "tile_idx", "tile_lse"):
+            assert np.array_equal(runs[B][k][:64], runs[64][k]), (B, k)
+    assert np.array_equal(runs[384]["tile_max"][:256], runs[256]["tile_max"])
+
+
 def test_graph_replay_matches_eager():
     p = make_problem(8, 64, 3000, T=1.0, seed=8)
     eager = run_device(p, offset=4)["idx"]
