@@ -322,10 +322,11 @@ def run_ours(args):
             extensions[f"topk{K}_us_per_call"] = round(us_tk, 2)
             del tk_out, tk_ws
 
-    # End to end through the C ABI: each step's inputs (H, temperatures, seeds,
-    # mask) go host -> device in one copy from one pinned buffer, fs_sample runs from
-    # an argument block built once (only the offset changes), and the sampled
-    # ids come back device -> host before the next step starts.
+    # End to end through the C ABI, one fs_sample_host call per step: the
+    # step's inputs (H, temperatures, seeds, mask) go host -> device in one copy
+    # from one pinned buffer, the sampling kernel runs from an argument block
+    # built once (only the offset changes), and the sampled ids come back
+    # device -> host (pinned) before the call returns and the next step starts.
     import ctypes
     lib = fs.load_library()
     parts = [inp["H"].contiguous().view(torch.uint8).view(-1),
@@ -360,14 +361,14 @@ def run_ours(args):
         out_tile_lse=tiles["out_tile_lse"].data_ptr() if tiles else None)
     args_ref = ctypes.byref(args_c)
     sh = ctypes.c_void_p(stream.cuda_stream)
+    hp, dp = ctypes.c_void_p(host_in.data_ptr()), ctypes.c_void_p(dev_in.data_ptr())
+    op, n_in = ctypes.c_void_p(out_h.data_ptr()), host_in.numel()
 
     def e2e_step(k):
-        dev_in.copy_(host_in, non_blocking=True)
         args_c.offset = k
-        if lib.fs_sample(args_ref, sh) != fs.FS_OK:
-            raise SystemExit("fs_sample failed")
-        out_h.copy_(out, non_blocking=True)
-        stream.synchronize()  # the sampled ids feed the next decode step
+        # sync=1: the sampled ids feed the next decode step
+        if lib.fs_sample_host(args_ref, hp, dp, n_in, op, 1, sh) != fs.FS_OK:
+            raise SystemExit("fs_sample_host failed")
 
     for k in range(3):
         e2e_step(k)

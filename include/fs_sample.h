@@ -169,6 +169,23 @@ fs_status fs_sample(const fs_sample_args *args, void *stream);
  */
 fs_status fs_sample_noalloc(const fs_sample_args *args, void *stream);
 
+/*
+ * One decode step from host memory: the end-to-end form of fs_sample, in one
+ * call.  Enqueues on `stream`, in order: a copy of in_bytes from host_in (host
+ * memory; pinned, for the copy to be asynchronous) to dev_in (device memory),
+ * the fs_sample call described by args -- whose input pointers the caller has
+ * pointed into dev_in, or anywhere else on the device -- and a copy of the B
+ * sampled ids from args->out_idx (required) to host_out (host int64 [B],
+ * pinned).  With sync != 0 it then waits for the stream, so the ids are in
+ * host_out when it returns FS_OK.  in_bytes may be 0 (inputs already on the
+ * device).  Errors: FS_ERR_INVALID_ARG for a null args, args->out_idx or
+ * host_out, or a null host_in / dev_in with in_bytes > 0; every error of
+ * fs_sample's argument checks -- both before anything is enqueued; FS_ERR_CUDA
+ * for a failed copy, launch or wait.
+ */
+fs_status fs_sample_host(const fs_sample_args *args, const void *host_in, void *dev_in,
+                         size_t in_bytes, int64_t *host_out, int sync, void *stream);
+
 /* Largest K of fs_sample_topk. */
 #define FS_TOPK_MAX 16
 

@@ -70,6 +70,9 @@ def load_library(path: str = LIB_PATH):
     lib.fs_sample.restype = ctypes.c_int
     lib.fs_sample_noalloc.argtypes = [ctypes.POINTER(FsSampleArgs), _c_ptr]
     lib.fs_sample_noalloc.restype = ctypes.c_int
+    lib.fs_sample_host.argtypes = [ctypes.POINTER(FsSampleArgs), _c_ptr, _c_ptr, ctypes.c_size_t,
+                                   _c_ptr, ctypes.c_int, _c_ptr]
+    lib.fs_sample_host.restype = ctypes.c_int
     lib.fs_gumbel_noise.argtypes = [_c_ptr, _c_u64, _c_u64, _c_i64, _c_i64, _c_i64, _c_i64,
                                     _c_ptr, _c_ptr]
     lib.fs_gumbel_noise.restype = ctypes.c_int
@@ -195,6 +198,38 @@ def fs_sample(H, W, *, temperature=None, vocab_mask=None, seeds=None, seed=0, of
     if st != FS_OK:
         raise FsError(st, "fs_sample")
     return out_idx
+
+
+def fs_sample_host(args, host_in, dev_in, host_out, *, sync=True, stream=None, device=None):
+    """One decode step from host memory (the C entry point of the same name):
+    copy host_in (pinned uint8 host tensor) to dev_in (uint8 device tensor of
+    at least the same size), run fs_sample with ``args`` (an FsSampleArgs
+    whose input pointers point into dev_in, or elsewhere on the device), copy
+    the B sampled ids to host_out (pinned int64 [B] host tensor) and, with
+    ``sync``, wait for them.  host_in may be None (nothing to copy).  Pass
+    ``args`` by reference (``ctypes.byref``) to reuse one argument block."""
+    lib = load_library()
+    device = torch.device(device or "cuda")
+    n = 0 if host_in is None else host_in.numel() * host_in.element_size()
+    if host_in is not None and (host_in.is_cuda or not dev_in.is_cuda
+                                or dev_in.numel() * dev_in.element_size() < n):
+        raise FsError(FS_ERR_INVALID_ARG, "host_in must be host memory no larger than dev_in")
+    if host_out.is_cuda or host_out.dtype != torch.int64 or host_out.numel() < args_batch(args):
+        raise FsError(FS_ERR_INVALID_ARG, "host_out must be an int64 host tensor of B entries")
+    ref = args if isinstance(args, type(ctypes.byref(FsSampleArgs()))) else ctypes.byref(args)
+    with torch.cuda.device(device):
+        st = lib.fs_sample_host(ref, _ptr(host_in), _ptr(dev_in) if host_in is not None else None,
+                                n, _ptr(host_out), 1 if sync else 0,
+                                _stream_handle(stream, device))
+    if st != FS_OK:
+        raise FsError(st, "fs_sample_host")
+    return host_out
+
+
+def args_batch(args) -> int:
+    """B of an FsSampleArgs (or of a ctypes reference to one)."""
+    obj = getattr(args, "_obj", args)
+    return int(obj.B)
 
 
 def fs_topk_workspace_size(B: int, V: int, K: int) -> int:

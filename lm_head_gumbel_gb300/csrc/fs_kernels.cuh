@@ -79,6 +79,7 @@ struct Stage1Params {
   int32_t* tile_idx;
   float* tile_lse;
   int64_t* out_idx;            // sampled ids, or null (per-tile outputs only)
+  int64_t* out_idx_host;       // optional second copy of the ids in mapped host memory
   float* out_max;              // optional: the row's largest noisy score
   int32_t vocab_offset;        // global id of W's first row (a multiple of 4)
   unsigned long long* row_keys;  // [B] packed (score, id) maxima, zero between calls
@@ -376,7 +377,9 @@ __device__ __forceinline__ void finish_rows(const Stage1Params& p) {
     __threadfence();
     for (int r = threadIdx.x; r < p.B; r += blockDim.x) {
       const unsigned long long key = atomicExch(p.row_keys + r, 0ull);
-      p.out_idx[r] = unpack_idx(key);
+      const int64_t id = unpack_idx(key);
+      p.out_idx[r] = id;
+      if (p.out_idx_host != nullptr) p.out_idx_host[r] = id;
       if (p.out_max != nullptr) p.out_max[r] = unpack_score(key);
     }
   }
@@ -782,6 +785,24 @@ __global__ void wait_timeout_kernel(uint64_t limit_ns) {
   ptx::fence_barrier_init();
   const Waiter waiter{&abort_word, limit_ns};
   waiter.wait(&bar, 0);  // phase 0 never completes
+}
+
+// Copy n bytes from mapped (pinned) host memory to device memory with SM
+// loads over the host link: 16 bytes a thread when both ends are 16-byte
+// aligned, else byte by byte.
+__global__ void stage_in_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
+                                size_t n, int vec) {
+  const size_t tid = size_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  const size_t stride = size_t(gridDim.x) * blockDim.x;
+  if (vec) {
+    const size_t n16 = n / 16;
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+    for (size_t i = tid; i < n16; i += stride) d4[i] = s4[i];
+    for (size_t i = n16 * 16 + tid; i < n; i += stride) dst[i] = src[i];
+  } else {
+    for (size_t i = tid; i < n; i += stride) dst[i] = src[i];
+  }
 }
 
 // The noise stage 1 adds, element by element (diagnostic entry point).

@@ -279,7 +279,10 @@ fs_status run_stage1(const fs_sample_args* a, int mode, Stage1Params& p, cudaStr
 }  // namespace
 }  // namespace fs
 
-extern "C" fs_status fs_sample(const fs_sample_args* a, void* stream_ptr) {
+namespace fs {
+namespace {
+// Every host-side check of fs_sample (inputs, outputs, workspace).
+fs_status check_sample(const fs_sample_args* a) {
   const fs_status chk = check_inputs(a);
   if (chk != FS_OK) return chk;
   const int64_t B = a->B, V = a->V;
@@ -297,11 +300,25 @@ extern "C" fs_status fs_sample(const fs_sample_args* a, void* stream_ptr) {
     if (!a->workspace || a->workspace_bytes < need || !aligned(a->workspace, 256))
       return FS_ERR_WORKSPACE;
   }
+  return FS_OK;
+}
+}  // namespace
+}  // namespace fs
+
+namespace fs {
+namespace {
+// fs_sample, optionally also writing the ids to `out_idx_host` (a device
+// address of mapped host memory).
+fs_status sample(const fs_sample_args* a, int64_t* out_idx_host, void* stream_ptr) {
+  const fs_status chk = check_sample(a);
+  if (chk != FS_OK) return chk;
+  const int64_t B = a->B, V = a->V;
   Stage1Params p = {};
   p.tile_max = a->out_tile_max;
   p.tile_idx = a->out_tile_idx;
   p.tile_lse = a->out_tile_lse;
   p.out_idx = a->out_idx;
+  p.out_idx_host = out_idx_host;
   p.out_max = a->out_max;
   p.ticket = a->out_idx ? static_cast<uint32_t*>(a->workspace) : nullptr;
   p.row_keys = a->out_idx ? reinterpret_cast<unsigned long long*>(
@@ -311,6 +328,24 @@ extern "C" fs_status fs_sample(const fs_sample_args* a, void* stream_ptr) {
   const fs_status lst = run_stage1(a, a->out_tile_lse ? kModeLse : kModeSample, p, stream);
   if (lst != FS_OK || a->out_lse == nullptr) return lst;
   return launch_row_lse(a->out_tile_lse, a->temperature, B, fs_num_tiles(V), a->out_lse, stream);
+}
+
+// Device address of host memory the GPU can read and write directly (pinned
+// and mapped, as page-locked allocations are under unified addressing), or
+// null if `host` is not such memory.
+void* mapped_host(const void* host) {
+  cudaPointerAttributes at = {};
+  if (cudaPointerGetAttributes(&at, host) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+}  // namespace
+}  // namespace fs
+
+extern "C" fs_status fs_sample(const fs_sample_args* a, void* stream_ptr) {
+  return sample(a, nullptr, stream_ptr);
 }
 
 extern "C" size_t fs_topk_workspace_size(int64_t B, int64_t V, int64_t K) {
@@ -399,6 +434,55 @@ extern "C" fs_status fs_sample_noalloc(const fs_sample_args* a, void* stream_ptr
   b.workspace = scratch;
   b.workspace_bytes = FS_NOALLOC_SCRATCH_BYTES;
   return fs_sample(&b, stream_ptr);
+}
+
+extern "C" fs_status fs_sample_host(const fs_sample_args* a, const void* host_in, void* dev_in,
+                                    size_t in_bytes, int64_t* host_out, int sync,
+                                    void* stream_ptr) {
+  if (a == nullptr || host_out == nullptr || a->out_idx == nullptr) return FS_ERR_INVALID_ARG;
+  if (in_bytes > 0 && (host_in == nullptr || dev_in == nullptr)) return FS_ERR_INVALID_ARG;
+  const fs_status chk = check_sample(a);
+  if (chk != FS_OK) return chk;
+  int num_sms = 0;
+  const fs_status st = device_setup(&num_sms);
+  if (st != FS_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  // Inputs in: mapped host memory is read by SMs over the host link (on a
+  // Grace host, NVLink-C2C: several times the copy engine's rate for a
+  // decode-sized H); other host memory goes through cudaMemcpyAsync.
+  if (in_bytes > 0) {
+    const void* src = mapped_host(host_in);
+    if (src != nullptr) {
+      const int vec = (reinterpret_cast<uintptr_t>(src) % 16 == 0 &&
+                       reinterpret_cast<uintptr_t>(dev_in) % 16 == 0) ? 1 : 0;
+      const size_t per_block = 256u * (vec ? 16u : 1u);
+      size_t blocks = (in_bytes + per_block - 1) / per_block;
+      if (blocks > size_t(num_sms) * 4u) blocks = size_t(num_sms) * 4u;
+      stage_in_kernel<<<unsigned(blocks), 256, 0, stream>>>(
+          static_cast<const uint8_t*>(src), static_cast<uint8_t*>(dev_in), in_bytes, vec);
+      if (cudaGetLastError() != cudaSuccess) return FS_ERR_CUDA;
+    } else if (cudaMemcpyAsync(dev_in, host_in, in_bytes, cudaMemcpyHostToDevice, stream) !=
+               cudaSuccess) {
+      cudaGetLastError();
+      return FS_ERR_CUDA;
+    }
+  }
+  // Ids out: the kernel's last CTA writes them to mapped host memory as well;
+  // otherwise they are copied back.
+  int64_t* out_mapped = static_cast<int64_t*>(mapped_host(host_out));
+  const fs_status run = sample(a, out_mapped, stream_ptr);
+  if (run != FS_OK) return run;
+  if (out_mapped == nullptr &&
+      cudaMemcpyAsync(host_out, a->out_idx, size_t(a->B) * sizeof(int64_t),
+                      cudaMemcpyDeviceToHost, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return FS_ERR_CUDA;
+  }
+  if (sync && cudaStreamSynchronize(stream) != cudaSuccess) {
+    cudaGetLastError();
+    return FS_ERR_CUDA;
+  }
+  return FS_OK;
 }
 
 extern "C" fs_status fs_gumbel_noise(const uint64_t* seeds, uint64_t seed, uint64_t offset,

@@ -33,7 +33,7 @@ def test_header_declares_entry_points():
     for want in ("fs_sample", "fs_workspace_size", "fs_num_tiles", "fs_status_string",
                  "fs_gumbel_noise", "fs_last_device_error", "fs_group_merge", "fs_online_merge",
                  "fs_sample_noalloc", "fs_wait_timeout_selftest", "fs_sample_topk",
-                 "fs_topk_workspace_size"):
+                 "fs_topk_workspace_size", "fs_sample_host"):
         assert want in names
 
 
@@ -161,3 +161,19 @@ def test_topk_workspace_and_bad_arguments(lib):
     assert f(ctypes.byref(_args(**dict(good, workspace_bytes=100))), 4, o, None, None) == 5
     assert f(ctypes.byref(_args(**dict(good, workspace=None))), 4, o, None, None) == 5
     assert f(None, 4, o, None, None) == 1
+
+
+def test_host_step_bad_arguments(lib):
+    """fs_sample_host checks its own buffers and every fs_sample argument
+    before it enqueues anything (so these return without touching CUDA)."""
+    p = ctypes.c_void_p
+    hin, din, hout = p(0x1000), p(0x2000), p(0x3000)
+    ws = dict(out_tile_max=None, out_tile_idx=None, workspace=0x70000, workspace_bytes=4096)
+    f = lib.fs_sample_host
+    assert f(None, hin, din, 64, hout, 1, None) == 1                               # no args
+    assert f(ctypes.byref(_args(**ws)), hin, din, 64, None, 1, None) == 1          # no host_out
+    assert f(ctypes.byref(_args(**dict(ws, out_idx=None))), hin, din, 64, hout, 1, None) == 1
+    assert f(ctypes.byref(_args(**ws)), None, din, 64, hout, 1, None) == 1         # no host_in
+    assert f(ctypes.byref(_args(**ws)), hin, None, 64, hout, 1, None) == 1         # no dev_in
+    assert f(ctypes.byref(_args(**dict(ws, B=0))), hin, din, 64, hout, 1, None) == 1
+    assert f(ctypes.byref(_args(**dict(ws, workspace=None))), hin, din, 64, hout, 1, None) == 5

@@ -134,6 +134,54 @@ def test_rows_do_not_depend_on_the_batch(V):
     assert np.array_equal(runs[384]["tile_max"][:256], runs[256]["tile_max"])
 
 
+def test_host_step_matches_device_call():
+    """fs_sample_host (host inputs -> device -> sampled ids back in host
+    memory, one call) gives what fs_sample gives on the same inputs, with and
+    without the wait inside the call, and with nothing to copy in."""
+    B, d, V = 24, 128, 5000
+    p = make_problem(B, d, V, T="row-uniform", per_row_seeds=True, mask_frac=0.02, seed=14)
+    want = run_device(p, seed=5, offset=21, lse=False, tiles=False)["idx"]
+    parts = [p["H"].view(torch.uint8).reshape(-1), p["temperature"].view(torch.uint8),
+             p["seeds"].view(torch.uint8), p["vocab_mask"].view(torch.uint8).reshape(-1)]
+    sizes = [t.numel() for t in parts]
+    offs = np.concatenate([[0], np.cumsum([(n + 255) // 256 * 256 for n in sizes])])
+    host_in = torch.zeros(int(offs[-1]), dtype=torch.uint8).pin_memory()
+    for t, o, n in zip(parts, offs, sizes):
+        host_in[int(o):int(o) + n].copy_(t.cpu())
+    dev_in = torch.empty_like(host_in, device="cuda")
+    dptr = [dev_in.data_ptr() + int(o) for o in offs[:4]]
+    out = torch.empty(B, dtype=torch.int64, device="cuda")
+    ws = torch.zeros(fs.fs_workspace_size(B, V), dtype=torch.uint8, device="cuda")
+    args = fs.FsSampleArgs(H=dptr[0], W=p["W"].data_ptr(), temperature=dptr[1],
+                           vocab_mask=dptr[3], mask_ld=p["vocab_mask"].stride(0), seeds=dptr[2],
+                           seed=5, offset=21, B=B, d=d, V=V, ldh=d, ldw=d,
+                           out_idx=out.data_ptr(), workspace=ws.data_ptr(),
+                           workspace_bytes=ws.numel())
+    host_out = torch.full((B,), -7, dtype=torch.int64).pin_memory()
+    fs.fs_sample_host(args, host_in, dev_in, host_out)
+    assert np.array_equal(host_out.numpy(), want)
+    host_out.fill_(-7)
+    s = torch.cuda.Stream()
+    fs.fs_sample_host(args, host_in, dev_in, host_out, sync=False, stream=s)
+    s.synchronize()
+    assert np.array_equal(host_out.numpy(), want)
+    host_out.fill_(-7)
+    fs.fs_sample_host(args, None, None, host_out)  # inputs already on the device
+    assert np.array_equal(host_out.numpy(), want)
+    # pageable (unmapped) host buffers take the copy-engine path
+    dev_in.zero_()
+    paged_out = torch.full((B,), -7, dtype=torch.int64)
+    fs.fs_sample_host(args, host_in.clone(), dev_in, paged_out)
+    assert np.array_equal(paged_out.numpy(), want)
+    # an unaligned pinned source takes the byte-wise copy kernel
+    dev_in.zero_()
+    shifted = torch.zeros(host_in.numel() + 1, dtype=torch.uint8).pin_memory()
+    shifted[1:].copy_(host_in)
+    dev_in2 = torch.empty(host_in.numel() + 16, dtype=torch.uint8, device="cuda")
+    fs.fs_sample_host(args, shifted[1:], dev_in2[1:host_in.numel() + 1], host_out)
+    assert torch.equal(dev_in2[1:host_in.numel() + 1].cpu(), host_in)
+
+
 def test_graph_replay_matches_eager():
     p = make_problem(8, 64, 3000, T=1.0, seed=8)
     eager = run_device(p, offset=4)["idx"]
