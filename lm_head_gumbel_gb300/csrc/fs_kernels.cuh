@@ -36,6 +36,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <type_traits>
 
 #include "fs_noise.cuh"
 #include "fs_ptx.cuh"
@@ -288,13 +289,59 @@ __device__ __forceinline__ void topk_insert(float (&ts)[KC], int32_t (&ti)[KC], 
   }
 }
 
-// Top-K form of epilogue_tile: the KC largest noisy scores of the row's tile
-// and their global ids, best first (-inf / -1 past the unmasked count),
-// written to the workspace.  By the Gumbel-top-k property the K largest scores
-// of a row are K draws without replacement from softmax(l'), in draw order.
+// v[j] for a lane-varying j, without local memory: a 5-level select tree.
+__device__ __forceinline__ float select32(const float (&v)[32], uint32_t j) {
+  float a[16];
+#pragma unroll
+  for (int q = 0; q < 16; ++q) a[q] = (j & 16u) ? v[q + 16] : v[q];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) a[q] = (j & 8u) ? a[q + 8] : a[q];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) a[q] = (j & 4u) ? a[q + 4] : a[q];
+#pragma unroll
+  for (int q = 0; q < 2; ++q) a[q] = (j & 2u) ? a[q + 2] : a[q];
+  return (j & 1u) ? a[1] : a[0];
+}
+
+// A thread's running top-KC list for the row it is working on, across the
+// tiles of consecutive units with that row (a "stretch"); sorted best first,
+// in base-2 units for sampled rows.
+template <int KC>
+struct TopKState {
+  float s[KC];
+  int32_t i[KC];
+  int row = -1;        // the stretch's row, -1 before the first tile
+  int last_tile = -1;  // the slot the list is written to
+  bool greedy = false;
+};
+
+// Write the stretch's list to the workspace slot of its last tile (the
+// stretch's other tiles hold an empty list), in natural units.
+template <int KC>
+__device__ __forceinline__ void topk_flush(const Stage1Params& p, const TopKState<KC>& st) {
+  if (st.row < 0) return;
+  const int64_t o = (int64_t(st.row) * p.n_tiles + st.last_tile) * KC;
+#pragma unroll
+  for (int q = 0; q < KC; ++q) {
+    const float m = (st.greedy || st.i[q] < 0) ? st.s[q] : kLn2 * (st.s[q] - kLog2Ln2);
+    p.topk_score[o + q] = m;
+    p.topk_idx[o + q] = st.i[q];
+  }
+}
+
+// Top-K form of epilogue_tile.  By the Gumbel-top-k property the K largest
+// noisy scores of a row are K draws without replacement from softmax(l'), in
+// draw order.  Each thread keeps the KC best (score, id) of everything it has
+// seen of its row; an element enters only if it beats the list's last entry,
+// which is safe because an element of the row's K <= KC best is among the KC
+// best of any subset holding it.  Per 32-id chunk every lane marks its
+// entering candidates, then the warp runs as many insertion rounds as the
+// lane with most candidates needs (one candidate per lane and round, lowest
+// id first, so ties keep the lower id), instead of one warp-wide insertion
+// per id that any lane wants.
 template <int KC>
 __device__ __forceinline__ void epilogue_tile_topk(const Stage1Params& p, uint32_t taddr,
-                                                   int row, int tile) {
+                                                   int row, int tile, TopKState<KC>& st) {
   const bool valid_row = row < p.B;
   float T = 1.0f;
   uint64_t seed = p.seed;
@@ -303,60 +350,69 @@ __device__ __forceinline__ void epilogue_tile_topk(const Stage1Params& p, uint32
     if (p.temperature) T = p.temperature[row];
     if (p.seeds) seed = p.seeds[row];
     if (p.mask) mrow = p.mask + int64_t(row) * p.mask_ld;
+    if (st.row != row) {  // a new stretch
+      topk_flush<KC>(p, st);
+#pragma unroll
+      for (int q = 0; q < KC; ++q) {
+        st.s[q] = -INFINITY;
+        st.i[q] = -1;
+      }
+      st.row = row;
+    }
+    const int64_t o = (int64_t(row) * p.n_tiles + tile) * KC;
+    p.topk_score[o] = -INFINITY;  // empty unless the stretch's list lands here
+    p.topk_idx[o] = -1;
+    st.last_tile = tile;
   }
   const bool greedy = !(T > 0.0f) || isinf(T);
+  st.greedy = greedy;
   const float scale2 = greedy ? 1.0f : kLog2e / T;
   const PhiloxSchedule ks(seed);
   const uint32_t ctr_row = static_cast<uint32_t>(row);
   const uint32_t ctr_lo = static_cast<uint32_t>(p.offset);
   const uint32_t ctr_hi = static_cast<uint32_t>(p.offset >> 32);
-  float ts[KC];
-  int32_t ti[KC];
-#pragma unroll
-  for (int q = 0; q < KC; ++q) {
-    ts[q] = -INFINITY;
-    ti[q] = -1;
-  }
   const int v_tile = tile * kTileV;
 #pragma unroll 1
   for (int c = 0; c < kTileV / 32; ++c) {
     uint32_t r[32];
     ptx::tmem_ld_32x32b_x32(taddr + uint32_t(c * 32), r);
     ptx::tmem_wait_ld();
-    if (!valid_row) continue;
     const int v0 = v_tile + c * 32;
-    uint32_t allow = mrow ? mrow[v0 >> 5] : 0xFFFFFFFFu;
-    const int n_in = p.V - v0;
-    if (n_in < 32) allow &= (n_in <= 0) ? 0u : ((1u << n_in) - 1u);
     const int32_t id0 = p.vocab_offset + v0;
-    if (greedy) {
+    float sc[32];
+    uint32_t cand = 0u;
+    if (valid_row) {
+      uint32_t allow = mrow ? mrow[v0 >> 5] : 0xFFFFFFFFu;
+      const int n_in = p.V - v0;
+      if (n_in < 32) allow &= (n_in <= 0) ? 0u : ((1u << n_in) - 1u);
+      if (greedy) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float l = __uint_as_float(r[j]);
-        if (((allow >> j) & 1u) && l > ts[KC - 1]) topk_insert<KC>(ts, ti, l, id0 + j);
+        for (int j = 0; j < 32; ++j) sc[j] = __uint_as_float(r[j]);
+      } else {
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          const uint4 rnd = philox4x32_10(
+              make_uint4(static_cast<uint32_t>(id0 >> 2) + g, ctr_row, ctr_lo, ctr_hi), ks);
+          const uint32_t words[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            sc[g * 4 + q] =
+                fmaf(__uint_as_float(r[g * 4 + q]), scale2, -gumbel_log2_from_word(words[q]));
+        }
       }
-      continue;
+      const float tau = st.s[KC - 1];
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        cand |= (((allow >> j) & 1u) && sc[j] > tau) ? (1u << j) : 0u;
     }
-#pragma unroll
-    for (int g = 0; g < 8; ++g) {
-      const uint4 rnd = philox4x32_10(
-          make_uint4(static_cast<uint32_t>(id0 >> 2) + g, ctr_row, ctr_lo, ctr_hi), ks);
-      const uint32_t words[4] = {rnd.x, rnd.y, rnd.z, rnd.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int j = g * 4 + i;
-        const float s2 = fmaf(__uint_as_float(r[j]), scale2, -gumbel_log2_from_word(words[i]));
-        if (((allow >> j) & 1u) && s2 > ts[KC - 1]) topk_insert<KC>(ts, ti, s2, id0 + j);
+    while (__any_sync(0xFFFFFFFFu, cand != 0u)) {
+      if (cand != 0u) {
+        const uint32_t j = uint32_t(__ffs(cand) - 1);
+        cand &= cand - 1u;
+        const float v = select32(sc, j);
+        if (v > st.s[KC - 1]) topk_insert<KC>(st.s, st.i, v, id0 + int32_t(j));
       }
     }
-  }
-  if (!valid_row) return;
-  const int64_t o = (int64_t(row) * p.n_tiles + tile) * KC;
-#pragma unroll
-  for (int q = 0; q < KC; ++q) {
-    const float m = (greedy || ti[q] < 0) ? ts[q] : kLn2 * (ts[q] - kLog2Ln2);
-    p.topk_score[o + q] = m;
-    p.topk_idx[o + q] = ti[q];
   }
 }
 
@@ -396,13 +452,27 @@ __host__ __device__ constexpr int topk_cap(int mode) {
   return mode == kModeTop4 ? 4 : mode == kModeTop16 ? 16 : 1;
 }
 
+// Per-thread epilogue state carried across units: the running top-K list in
+// the top-K modes, nothing otherwise.
+struct NoState {};
+template <int kMode>
+using EpilogueState =
+    typename std::conditional<(kMode == kModeTop4 || kMode == kModeTop16),
+                              TopKState<topk_cap(kMode)>, NoState>::type;
+
 template <int kMode>
 __device__ __forceinline__ void epilogue_unit(const Stage1Params& p, uint32_t taddr, int row,
-                                              int tile) {
+                                              int tile, EpilogueState<kMode>& st) {
   if constexpr (kMode == kModeSample || kMode == kModeLse)
     epilogue_tile<kMode == kModeLse>(p, taddr, row, tile);
   else
-    epilogue_tile_topk<topk_cap(kMode)>(p, taddr, row, tile);
+    epilogue_tile_topk<topk_cap(kMode)>(p, taddr, row, tile, st);
+}
+
+// After a thread's last unit: the top-K modes write the open stretch's list.
+template <int kMode>
+__device__ __forceinline__ void epilogue_finish(const Stage1Params& p, EpilogueState<kMode>& st) {
+  if constexpr (kMode == kModeTop4 || kMode == kModeTop16) topk_flush<topk_cap(kMode)>(p, st);
 }
 
 // Single-CTA stage 1: a unit is (vocabulary block vt of 256 ids, batch block mt
@@ -544,6 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;  // the tensor-memory lane quadrant this warp may read
     const int half = e >> 2;    // which 128-column half of the unit
     uint32_t acc = 0, acc_phase = 0;
+    EpilogueState<kMode> est;
     for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
       const int vt = unit / p.n_mt, mt = unit % p.n_mt;
       int ok = 0;
@@ -556,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (row0 < p.B && tile < p.n_tiles) {
         const uint32_t taddr =
             tmem_base + (uint32_t(quad * 32) << 16) + acc * kBlockN + uint32_t(half * kTileV);
-        epilogue_unit<kMode>(p, taddr, row0 + lane, tile);
+        epilogue_unit<kMode>(p, taddr, row0 + lane, tile, est);
       }
       ptx::tc_fence_before();
       __syncwarp();
@@ -564,6 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
+    epilogue_finish<kMode>(p, est);
   }
 
   ptx::tc_fence_before();
@@ -738,6 +810,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tempty_addr0 = ptx::cluster_addr(&tempty_bar[0], 0);
     const uint32_t tempty_addr1 = ptx::cluster_addr(&tempty_bar[1], 0);
     uint32_t acc = 0, acc_phase = 0;
+    EpilogueState<kMode> est;
     for (int u = pair_id; u < n_units; u += n_pairs) {
       const int vt = u / n_mp, mp = u % n_mp;
       int ok = 0;
@@ -750,7 +823,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (row0 < p.B && tile < p.n_tiles) {
         const uint32_t taddr =
             tmem_base + (uint32_t(quad * 32) << 16) + acc * kBlockN + uint32_t(half * kTileV);
-        epilogue_unit<kMode>(p, taddr, row0 + lane, tile);
+        epilogue_unit<kMode>(p, taddr, row0 + lane, tile, est);
       }
       ptx::tc_fence_before();
       __syncwarp();
@@ -758,6 +831,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
+    epilogue_finish<kMode>(p, est);
   }
 
   ptx::tc_fence_before();
