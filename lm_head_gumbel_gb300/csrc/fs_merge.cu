@@ -152,49 +152,40 @@ __device__ __forceinline__ bool precedes(float as, int32_t ai, float bs, int32_t
 
 constexpr int kTopkThreads = 256;
 
-// Each row's K best of its per-tile candidates (Gumbel-top-k: K draws without
-// replacement, in draw order).  One block per row.  Every tile's KC
-// candidates arrive sorted best first, so a thread walks each of its tiles
-// only until a candidate no longer makes its own KC-best list; then K rounds
-// pick the best remaining head across the block.
+// Merge a sorted list c into the sorted list l, keeping the KC best: the
+// better of l[q] and c[KC-1-q] for every q is a bitonic sequence holding the
+// KC best of both, which a bitonic merge network sorts.
 template <int KC>
-__global__ void __launch_bounds__(kTopkThreads)
-    topk_reduce_kernel(const float* __restrict__ cand_score,
-                       const int32_t* __restrict__ cand_idx, int32_t n_tiles, int32_t K,
-                       int64_t* __restrict__ out_idx, float* __restrict__ out_score) {
-  const int row = blockIdx.x;
-  const int64_t base = int64_t(row) * n_tiles * KC;
-  float ls[KC];
-  int32_t li[KC];
+__device__ __forceinline__ void list_merge(float (&ls)[KC], int32_t (&li)[KC],
+                                           const float (&cs)[KC], const int32_t (&ci)[KC]) {
 #pragma unroll
   for (int q = 0; q < KC; ++q) {
-    ls[q] = -INFINITY;
-    li[q] = -1;
+    const bool take = precedes(cs[KC - 1 - q], ci[KC - 1 - q], ls[q], li[q]);
+    ls[q] = take ? cs[KC - 1 - q] : ls[q];
+    li[q] = take ? ci[KC - 1 - q] : li[q];
   }
-  for (int t = threadIdx.x; t < n_tiles; t += kTopkThreads) {
-    const float* ts = cand_score + base + int64_t(t) * KC;
-    const int32_t* ti = cand_idx + base + int64_t(t) * KC;
-    for (int q = 0; q < KC; ++q) {
-      const float sc = ts[q];
-      const int32_t ic = ti[q];
-      if (!precedes(sc, ic, ls[KC - 1], li[KC - 1])) break;  // the rest are worse
-      ls[KC - 1] = sc;
-      li[KC - 1] = ic;
 #pragma unroll
-      for (int u = KC - 1; u > 0; --u) {
-        const bool up = precedes(ls[u], li[u], ls[u - 1], li[u - 1]);
-        const float a = ls[u], b = ls[u - 1];
-        const int32_t ia = li[u], ib = li[u - 1];
-        ls[u - 1] = up ? a : b;
-        ls[u] = up ? b : a;
-        li[u - 1] = up ? ia : ib;
-        li[u] = up ? ib : ia;
-      }
+  for (int st = KC / 2; st > 0; st >>= 1) {
+#pragma unroll
+    for (int q = 0; q < KC; ++q) {
+      if ((q & st) != 0) continue;
+      const int r = q + st;
+      const bool sw = precedes(ls[r], li[r], ls[q], li[q]);
+      const float a = ls[q], b = ls[r];
+      const int32_t ia = li[q], ib = li[r];
+      ls[q] = sw ? b : a;
+      ls[r] = sw ? a : b;
+      li[q] = sw ? ib : ia;
+      li[r] = sw ? ia : ib;
     }
   }
-  __shared__ float ws[kTopkThreads / 32];
-  __shared__ int32_t wi[kTopkThreads / 32];
-  __shared__ int32_t win_i;
+}
+
+// K rounds over the lanes' sorted lists: the best head of the warp, which its
+// holder pops.  Every lane receives the round's winner.
+template <int KC, typename Emit>
+__device__ __forceinline__ void warp_select(float (&ls)[KC], int32_t (&li)[KC], int K,
+                                            Emit emit) {
   for (int j = 0; j < K; ++j) {
     float bs = ls[0];
     int32_t bi = li[0];
@@ -207,23 +198,8 @@ __global__ void __launch_bounds__(kTopkThreads)
         bi = oi;
       }
     }
-    if ((threadIdx.x & 31) == 0) {
-      ws[threadIdx.x >> 5] = bs;
-      wi[threadIdx.x >> 5] = bi;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      for (int w = 1; w < kTopkThreads / 32; ++w)
-        if (precedes(ws[w], wi[w], bs, bi)) {
-          bs = ws[w];
-          bi = wi[w];
-        }
-      win_i = bi;
-      out_idx[int64_t(row) * K + j] = bi;
-      if (out_score != nullptr) out_score[int64_t(row) * K + j] = bi >= 0 ? bs : -INFINITY;
-    }
-    __syncthreads();
-    if (li[0] >= 0 && li[0] == win_i) {  // this thread held the winner: pop it
+    emit(j, bs, bi);
+    if (li[0] >= 0 && li[0] == bi) {  // ids are distinct: this lane held the winner
 #pragma unroll
       for (int q = 0; q < KC - 1; ++q) {
         ls[q] = ls[q + 1];
@@ -233,6 +209,95 @@ __global__ void __launch_bounds__(kTopkThreads)
       li[KC - 1] = -1;
     }
   }
+}
+
+// Each row's K best of its candidate lists (Gumbel-top-k: K draws without
+// replacement, in draw order).  One block per row.  Every slot holds a list
+// sorted best first (an empty list starts with id -1).  A thread reads the
+// heads of 8 of its slots at once, loads a whole list (16-byte loads) only
+// when its head makes the thread's own KC-best list, and merges it by a
+// bitonic network.  Then each warp picks its K best by shuffles, and warp 0
+// picks the row's K best from the warps' lists.
+template <int KC>
+__global__ void __launch_bounds__(kTopkThreads)
+    topk_reduce_kernel(const float* __restrict__ cand_score,
+                       const int32_t* __restrict__ cand_idx, int32_t n_tiles, int32_t K,
+                       int64_t* __restrict__ out_idx, float* __restrict__ out_score) {
+  static_assert(KC % 4 == 0, "lists are read 4 entries at a time");
+  constexpr int kWarps = kTopkThreads / 32;
+  constexpr int kGroup = 8;
+  const int row = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t base = int64_t(row) * n_tiles * KC;
+  float ls[KC];
+  int32_t li[KC];
+#pragma unroll
+  for (int q = 0; q < KC; ++q) {
+    ls[q] = -INFINITY;
+    li[q] = -1;
+  }
+  for (int t0 = threadIdx.x; t0 < n_tiles; t0 += kTopkThreads * kGroup) {
+    float hs[kGroup];
+    int32_t hi[kGroup];
+#pragma unroll
+    for (int g = 0; g < kGroup; ++g) {
+      const int t = t0 + g * kTopkThreads;
+      hs[g] = -INFINITY;
+      hi[g] = -1;
+      if (t < n_tiles) {
+        hs[g] = cand_score[base + int64_t(t) * KC];
+        hi[g] = cand_idx[base + int64_t(t) * KC];
+      }
+    }
+#pragma unroll 1
+    for (int g = 0; g < kGroup; ++g) {
+      float h_s = hs[0];  // hs[g] by selects: a dynamic index would go to local memory
+      int32_t h_i = hi[0];
+#pragma unroll
+      for (int x = 1; x < kGroup; ++x) {
+        h_s = g == x ? hs[x] : h_s;
+        h_i = g == x ? hi[x] : h_i;
+      }
+      if (!precedes(h_s, h_i, ls[KC - 1], li[KC - 1])) continue;
+      const int64_t o = base + int64_t(t0 + g * kTopkThreads) * KC;
+      const float4* s4 = reinterpret_cast<const float4*>(cand_score + o);
+      const int4* i4 = reinterpret_cast<const int4*>(cand_idx + o);
+      float cs[KC];
+      int32_t ci[KC];
+#pragma unroll
+      for (int q = 0; q < KC / 4; ++q) {
+        const float4 a = s4[q];
+        const int4 b = i4[q];
+        cs[4 * q] = a.x, cs[4 * q + 1] = a.y, cs[4 * q + 2] = a.z, cs[4 * q + 3] = a.w;
+        ci[4 * q] = b.x, ci[4 * q + 1] = b.y, ci[4 * q + 2] = b.z, ci[4 * q + 3] = b.w;
+      }
+      list_merge<KC>(ls, li, cs, ci);
+    }
+  }
+  // Each warp's K best, by shuffles.
+  __shared__ float ws[kWarps][KC];
+  __shared__ int32_t wi[kWarps][KC];
+  warp_select<KC>(ls, li, K, [&](int j, float bs, int32_t bi) {
+    if (lane == 0) {
+      ws[warp][j] = bs;
+      wi[warp][j] = bi;
+    }
+  });
+  __syncthreads();
+  if (warp != 0) return;
+  // The row's K best from the warps' lists (lane w holds warp w's).
+#pragma unroll
+  for (int q = 0; q < KC; ++q) {
+    const bool has = lane < kWarps && q < K;
+    ls[q] = has ? ws[lane][q] : -INFINITY;
+    li[q] = has ? wi[lane][q] : -1;
+  }
+  warp_select<KC>(ls, li, K, [&](int j, float bs, int32_t bi) {
+    if (lane == 0) {
+      out_idx[int64_t(row) * K + j] = bi;
+      if (out_score != nullptr) out_score[int64_t(row) * K + j] = bi >= 0 ? bs : -INFINITY;
+    }
+  });
 }
 
 }  // namespace

@@ -119,6 +119,28 @@ def test_topk_pairs_follow_plackett_luce():
     assert pval > 1e-3, pval
 
 
+@pytest.mark.parametrize("B,V", [(384, 5000), (512, 3000), (136, 40000)])
+def test_topk_rows_changing_between_units(B, V):
+    """Batches whose epilogue threads change rows from unit to unit (three
+    128-row blocks on single CTAs; two 256-row pair blocks) or run long
+    stretches of one row (136 rows, 313 tiles): the running per-thread lists
+    are flushed at every row change; every row's first id is fs_sample's and
+    sampled rows match the oracle."""
+    K = 16
+    p = make_problem(B, 64, V, T="row-uniform", per_row_seeds=True, seed=60 + B)
+    idx, score = device_topk(p, K, offset=4)
+    one = fs.fs_sample(p["H"], p["W"], temperature=p["temperature"], seeds=p["seeds"], seed=7,
+                       offset=4)
+    torch.cuda.synchronize()
+    assert np.array_equal(idx[:, 0], one.cpu().numpy())
+    assert np.all(np.diff(score, axis=1) <= 0)
+    for b in range(B):
+        got = idx[b][idx[b] >= 0]
+        assert len(set(got.tolist())) == len(got) == K
+    rows = sorted({r for r in (0, 127, 128, 255, 256, B - 1) if r < B})
+    assert check_against_oracle(p, K, idx, score, rows=rows, offset=4) >= len(rows) * K * 0.7
+
+
 @pytest.mark.parametrize("B,K", [(64, 8), (256, 16)])
 def test_topk_full_size_head(B, K):
     """Qwen3-8B-shaped head (d=4096, V=151936): the single-CTA kernel (B=64)
