@@ -217,20 +217,26 @@ __device__ __forceinline__ void epilogue_tile(const Stage1Params& p, uint32_t ta
     uint32_t r[32];
     ptx::tmem_ld_32x32b_x32(taddr + uint32_t(c * 32), r);
     ptx::tmem_wait_ld();
-    if (!valid_row) continue;
     const int v0 = v_tile + c * 32;
-    uint32_t allow = mrow ? mrow[v0 >> 5] : 0xFFFFFFFFu;
-    const int n_in = p.V - v0;
-    if (n_in < 32) allow &= (n_in <= 0) ? 0u : ((1u << n_in) - 1u);
+    uint32_t allow = 0xFFFFFFFFu;
+    if (valid_row) {
+      if (mrow) allow = mrow[v0 >> 5];
+      const int n_in = p.V - v0;
+      if (n_in < 32) allow &= (n_in <= 0) ? 0u : ((1u << n_in) - 1u);
+    }
+    // The mask test is skipped only when no lane of the warp needs it: a
+    // per-lane choice would run both forms one after the other.
+    const bool unmasked = __all_sync(0xFFFFFFFFu, allow == 0xFFFFFFFFu);
+    if (!valid_row) continue;
     int best_j = -1;
     if (greedy) {
-      if (allow == 0xFFFFFFFFu)
+      if (unmasked)
         greedy_chunk<false>(r, allow, best, best_j);
       else
         greedy_chunk<true>(r, allow, best, best_j);
     } else {
       const uint32_t ctr0 = static_cast<uint32_t>((p.vocab_offset + v0) >> 2);
-      if (allow == 0xFFFFFFFFu)
+      if (unmasked)
         sample_chunk<false>(r, allow, scale2, ctr0, ctr_row, ctr_lo, ctr_hi, ks, best, best_j);
       else
         sample_chunk<true>(r, allow, scale2, ctr0, ctr_row, ctr_lo, ctr_hi, ks, best, best_j);
