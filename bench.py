@@ -489,9 +489,20 @@ def cpu_baseline(inp, B, budget_s):
     t0 = time.perf_counter()
     o.sample(Hb, Wb, temperature=T, seeds=S, mask=M, rows=rows)
     per_row = (time.perf_counter() - t0) / n if n else first
-    return {"value": round(per_row * B * 1e6, 1), "unit": "us/call", "cores": o.num_threads(),
+    cores = o.num_threads()
+    # the same oracle on one core: one row
+    o.set_num_threads(1)
+    try:
+        t0 = time.perf_counter()
+        o.sample(Hb, Wb, temperature=T, seeds=S, mask=M, rows=[0])
+        one_core_row = time.perf_counter() - t0
+    finally:
+        o.set_num_threads(cores)
+    return {"value": round(per_row * B * 1e6, 1), "unit": "us/call", "cores": cores,
             "kind": "oracle",
-            "sample": f"{n} of the call's {B} rows (fp64, full vocabulary each), scaled to {B} rows"}
+            "sample": f"{n} of the call's {B} rows (fp64, full vocabulary each), scaled to {B} rows",
+            "single_core": {"value": round(one_core_row * B * 1e6, 1), "unit": "us/call",
+                            "sample": f"1 row on 1 core, scaled to {B} rows"}}
 
 
 def run_reference(args):

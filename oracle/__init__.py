@@ -67,6 +67,8 @@ class Oracle:
         L.fso_sample_rows.restype = ctypes.c_int
         L.fso_num_threads.argtypes = []
         L.fso_num_threads.restype = ctypes.c_int
+        L.fso_set_num_threads.argtypes = [ctypes.c_int]
+        L.fso_set_num_threads.restype = None
 
     # ---- scalar pieces ---------------------------------------------------
     def philox(self, counter, key):
@@ -103,6 +105,10 @@ class Oracle:
 
     def num_threads(self) -> int:
         return self.lib.fso_num_threads()
+
+    def set_num_threads(self, n: int) -> None:
+        """Threads of the OpenMP regions from now on (results do not depend on it)."""
+        self.lib.fso_set_num_threads(int(n))
 
     # ---- the definition ------------------------------------------------------
     def logits(self, H, W):

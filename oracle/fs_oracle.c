@@ -276,10 +276,13 @@ int fso_sample_rows(const uint16_t *H, const uint16_t *W, int64_t B, int64_t d,
   return 0;
 }
 
-/* Threads an OpenMP parallel region of this build uses (1 without OpenMP). */
+/* Threads an OpenMP parallel region of this build uses (1 without OpenMP),
+ * and a setter for it (timing only; the results do not depend on it). */
 #ifdef _OPENMP
 #include <omp.h>
 int fso_num_threads(void) { return omp_get_max_threads(); }
+void fso_set_num_threads(int n) { if (n > 0) omp_set_num_threads(n); }
 #else
 int fso_num_threads(void) { return 1; }
+void fso_set_num_threads(int n) { (void)n; }
 #endif

@@ -231,6 +231,25 @@ def test_chi_square_on_device():
     assert agree > 0.9 * (n // 10)
 
 
+def test_max_stability_on_device():
+    """Max-stability of the device's per-tile outputs: over independent rows
+    (the same logits, per-row seeds) m_t - L_t is Gumbel(0, 1) for every tile
+    (mean Euler's gamma, Kolmogorov-Smirnov against the Gumbel cdf); this ties
+    the noise, the max and the tile log-sum-exp together."""
+    import scipy.stats
+    B, d, V = 4096, 32, 512
+    p = make_problem(1, d, V, T=0.9, seed=15)
+    H = p["H"].expand(B, d).contiguous()  # one row of logits, B independent draws
+    temperature = p["temperature"].expand(B).contiguous()
+    seeds = wl.make_seeds(B, base=77, device="cuda")
+    q = {"H": H, "W": p["W"], "temperature": temperature, "seeds": seeds, "vocab_mask": None}
+    dev = run_device(q, offset=3)
+    x = (dev["tile_max"] - dev["tile_lse"]).astype(np.float64)
+    for t in range(x.shape[1]):
+        assert abs(x[:, t].mean() - oracle.EULER_GAMMA) < 4.5 * math.sqrt(oracle.GUMBEL_VAR / B)
+        assert scipy.stats.kstest(x[:, t], scipy.stats.gumbel_r.cdf).pvalue > 1e-3, t
+
+
 def test_group_merge_on_device_tiles():
     """Group-Gumbel-Max over 4 vocabulary partitions, fed the device's per-tile
     (max, argmax, log-sum-exp), reproduces the distribution, and the exact
