@@ -201,9 +201,11 @@ size_t fs_topk_workspace_size(int64_t B, int64_t V, int64_t K);
  * replacement from softmax(l'[b, :]) (the aitrends.kr write-up notes the design
  * extends to top-k); out_topk_idx[b, 0] is the id fs_sample returns for the
  * same inputs.  Greedy rows give the K largest logits.  The stage-1 kernel
- * keeps the best 4 (K <= 4) or 16 (K <= 16) scores of every (row, 128-id tile)
- * in the workspace (args->workspace, fs_topk_workspace_size bytes, 256-byte
- * aligned, no initialisation needed) and a second kernel merges them per row.
+ * writes candidate lists -- the best 4 (K <= 4) or 16 (K <= 16) scores of each
+ * run of tiles one thread saw of a row, in one (row, 128-id tile) slot of the
+ * workspace, the run's other slots left empty -- to args->workspace
+ * (fs_topk_workspace_size bytes, 256-byte aligned, no initialisation needed),
+ * and a second kernel merges them per row.
  * Uses args' inputs (H, W, temperature, mask, seeds, offset, vocab_offset);
  * args' outputs (out_idx, out_tile_*, out_max, out_lse) must be NULL.
  * out_topk_idx: int64 [B, K] (-1 past the row's unmasked count);
