@@ -94,7 +94,20 @@ struct Stage1Params {
   // stages, so more of W is in flight.
   uint32_t n_stages;
   uint32_t stage_bytes;
+  // Launched to overlap the kernel that writes H and the per-row inputs
+  // (programmatic dependent launch): W streams at once, H and the per-row
+  // inputs are read only after the grid dependency is resolved.
+  uint32_t pdl;
 };
+
+// The producer's H copies of the first ring fill, held back until the grid
+// dependency is resolved when the kernel overlaps the one writing H.
+struct DeferredH {
+  int n = 0;
+  uint32_t stage[8];
+  int kb[8], row[8];
+};
+static_assert(kMaxStages <= 8, "a ring fill of deferred H copies fits DeferredH");
 
 // Bounded mbarrier waits: past the limit the CTA raises its abort flag and
 // the device error word, and every role winds down instead of spinning.
@@ -539,6 +552,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_h = ptx::policy_evict_last();
       uint32_t stage = 0, phase = 0, issued = 0;
       bool ok = true;
+      bool deferring = p.pdl != 0;
+      DeferredH defer;
+      auto flush_h = [&]() {
+        ptx::grid_dependency_wait();
+        for (int i = 0; i < defer.n; ++i)
+          ptx::tma_load_2d(smem + size_t(defer.stage[i]) * p.stage_bytes, &tmap_h,
+                           &full_bar[defer.stage[i]], defer.kb[i] * kBlockK, defer.row[i], pol_h);
+        defer.n = 0;
+        deferring = false;
+      };
       for (int unit = blockIdx.x; ok && unit < n_units; unit += gridDim.x) {
         const int vt = unit / p.n_mt, mt = unit % p.n_mt;
         // Each vocabulary block starts its K loop at its own slice, so CTAs
@@ -557,14 +580,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::mbar_arrive_expect_tx(&full_bar[stage], h_bytes + kSmemB);
           ptx::tma_load_2d(sa + h_bytes, &tmap_w, &full_bar[stage], kb * kBlockK, vt * kBlockN,
                            pol_w);
-          ptx::tma_load_2d(sa, &tmap_h, &full_bar[stage], kb * kBlockK, mt * kBlockM, pol_h);
+          if (deferring) {
+            defer.stage[defer.n] = stage;
+            defer.kb[defer.n] = kb;
+            defer.row[defer.n++] = mt * kBlockM;
+          } else {
+            ptx::tma_load_2d(sa, &tmap_h, &full_bar[stage], kb * kBlockK, mt * kBlockM, pol_h);
+          }
           ++issued;
           if (++stage == p.n_stages) {
             stage = 0;
             phase ^= 1u;
           }
+          if (deferring && defer.n == int(p.n_stages)) flush_h();
         }
       }
+      if (deferring) flush_h();
       // Every issued copy must land before the CTA (and its shared memory)
       // goes away: wait for the last fill of each stage.
       for (uint32_t s = 0; s < p.n_stages; ++s) {
@@ -616,6 +647,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ---------------- epilogue ----------------
+    if (p.pdl) ptx::grid_dependency_wait();  // the per-row inputs may still be in flight
     const int e = warp - 2;
     const int quad = warp & 3;  // the tensor-memory lane quadrant this warp may read
     const int half = e >> 2;    // which 128-column half of the unit
@@ -666,6 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // CTAs' barriers.  Each CTA's epilogue reads its own 128 rows; the leader's
 // "tensor memory empty" barrier collects the epilogue warps of both CTAs.
 constexpr int kPairStages = 6;
+static_assert(kPairStages <= 8, "a ring fill of deferred H copies fits DeferredH");
 constexpr uint32_t kPairSmemA = 128 * kBlockK * 2;  // 16 KB: this CTA's batch rows
 constexpr uint32_t kPairSmemB = 128 * kBlockK * 2;  // 16 KB: this CTA's vocabulary rows
 constexpr uint32_t kPairStageBytes = kPairSmemA + kPairSmemB;
@@ -733,6 +766,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_h = ptx::policy_evict_last();
       uint32_t stage = 0, phase = 0, issued = 0;
       bool ok = true;
+      bool deferring = p.pdl != 0;
+      DeferredH defer;
+      auto flush_h = [&]() {
+        ptx::grid_dependency_wait();
+        for (int i = 0; i < defer.n; ++i)
+          ptx::tma_load_2d_pair(smem + size_t(defer.stage[i]) * kPairStageBytes, &tmap_h,
+                                ptx::cluster_addr(&full_bar[defer.stage[i]], 0),
+                                defer.kb[i] * kBlockK, defer.row[i], pol_h);
+        defer.n = 0;
+        deferring = false;
+      };
       for (int u = pair_id; ok && u < n_units; u += n_pairs) {
         const int vt = u / n_mp, mp = u % n_mp;
         const int k_start =
@@ -752,14 +796,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t full_addr = ptx::cluster_addr(&full_bar[stage], 0);
           if (leader) ptx::mbar_arrive_expect_tx(&full_bar[stage], 2 * kPairStageBytes);
           ptx::tma_load_2d_pair(sa + kPairSmemA, &tmap_w, full_addr, kb * kBlockK, w_y, pol_w);
-          ptx::tma_load_2d_pair(sa, &tmap_h, full_addr, kb * kBlockK, a_y, pol_h);
+          if (deferring) {
+            defer.stage[defer.n] = stage;
+            defer.kb[defer.n] = kb;
+            defer.row[defer.n++] = a_y;
+          } else {
+            ptx::tma_load_2d_pair(sa, &tmap_h, full_addr, kb * kBlockK, a_y, pol_h);
+          }
           ++issued;
           if (++stage == kPairStages) {
             stage = 0;
             phase ^= 1u;
           }
+          if (deferring && defer.n == kPairStages) flush_h();
         }
       }
+      if (deferring) flush_h();
       // The leader's full barriers see both CTAs' copies land; wait for the
       // last fill of each stage before anything goes away.
       if (leader) {
@@ -810,6 +862,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ---------------- epilogue (both CTAs) ----------------
+    if (p.pdl) ptx::grid_dependency_wait();  // the per-row inputs may still be in flight
     const int e = warp - 2;
     const int quad = warp & 3;
     const int half = e >> 2;
@@ -872,6 +925,7 @@ __global__ void wait_timeout_kernel(uint64_t limit_ns) {
 // aligned, else byte by byte.
 __global__ void stage_in_kernel(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
                                 size_t n, int vec) {
+  ptx::grid_launch_dependents();  // the sampling kernel may start streaming W now
   const size_t tid = size_t(blockIdx.x) * blockDim.x + threadIdx.x;
   const size_t stride = size_t(gridDim.x) * blockDim.x;
   if (vec) {

@@ -70,6 +70,19 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, ui
       : "memory");
 }
 
+// ---- programmatic dependent launch -----------------------------------------
+// Wait until the grids this one depends on have completed and their memory is
+// visible (returns at once when the launch had no such dependency).
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Let the grid launched after this one (with programmatic serialization)
+// start before this one ends.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- thread-block clusters ------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;

@@ -38,18 +38,30 @@ EncodeTiledFn g_encode = nullptr;
 thread_local const DeviceState* g_last_state = nullptr;  // set by device_setup
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
+// attr must hold two entries: the cluster shape (cluster > 1) and, with pdl,
+// programmatic stream serialization (the kernel may start before the previous
+// one on the stream ends; it resolves the dependency itself).
 cudaLaunchConfig_t launch_config(int cluster, cudaLaunchAttribute* attr, cudaStream_t stream,
-                                 size_t smem) {
+                                 size_t smem, bool pdl = false) {
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = unsigned(cluster);
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  unsigned n = 0;
+  if (cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = unsigned(cluster);
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = cluster > 1 ? 1 : 0;
+  cfg.numAttrs = n;
   return cfg;
 }
 
@@ -65,7 +77,7 @@ bool prepare_mode(DeviceState& st, int sms) {
   if (cudaFuncSetAttribute(pk, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            int(kPairSmemBytes)) != cudaSuccess)
     return false;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = launch_config(2, attr, nullptr, kPairSmemBytes);
   cfg.gridDim = dim3(unsigned((sms / 2) * 2), 1, 1);
   int n = 0;
@@ -78,18 +90,18 @@ template <int kMode>
 fs_status launch_mode(bool pair, const CUtensorMap& tmap_h, const CUtensorMap& tmap_w,
                       const Stage1Params& p, const DeviceState& ds, cudaStream_t stream) {
   const int n_vt = int((int64_t(p.V) + kBlockN - 1) / kBlockN);
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaError_t err;
   if (pair) {
     const int n_units = n_vt * int((int64_t(p.B) + 2 * kBlockM - 1) / (2 * kBlockM));
     const int pairs = n_units < ds.max_pairs[kMode] ? n_units : ds.max_pairs[kMode];
-    cudaLaunchConfig_t cfg = launch_config(2, attr, stream, kPairSmemBytes);
+    cudaLaunchConfig_t cfg = launch_config(2, attr, stream, kPairSmemBytes, p.pdl != 0);
     cfg.gridDim = dim3(unsigned(pairs * 2), 1, 1);
     err = cudaLaunchKernelEx(&cfg, stage1_pair_kernel<kMode>, tmap_h, tmap_w, p);
   } else {
     const int n_units = n_vt * p.n_mt;
     const int grid = n_units < ds.num_sms ? n_units : ds.num_sms;
-    cudaLaunchConfig_t cfg = launch_config(1, attr, stream, kSmemBytes);
+    cudaLaunchConfig_t cfg = launch_config(1, attr, stream, kSmemBytes, p.pdl != 0);
     cfg.gridDim = dim3(unsigned(grid), 1, 1);
     err = cudaLaunchKernelEx(&cfg, stage1_kernel<kMode>, tmap_h, tmap_w, p);
   }
@@ -229,7 +241,8 @@ fs_status check_inputs(const fs_sample_args* a) {
 // Encode the tensor maps, fill the kernel parameters and launch the stage-1
 // kernel of `mode` (single CTAs, or CTA pairs for an even number of 128-row
 // batch blocks).  `p` arrives with the output pointers set.
-fs_status run_stage1(const fs_sample_args* a, int mode, Stage1Params& p, cudaStream_t stream) {
+fs_status run_stage1(const fs_sample_args* a, int mode, Stage1Params& p, cudaStream_t stream,
+                     bool pdl = false) {
   int num_sms = 0;
   const fs_status st = device_setup(&num_sms);
   if (st != FS_OK) return st;
@@ -264,6 +277,7 @@ fs_status run_stage1(const fs_sample_args* a, int mode, Stage1Params& p, cudaStr
   p.vocab_offset = int32_t(a->vocab_offset);
   p.wait_limit_ns = kWaitLimitNs;
   p.h_box_rows = h_rows;
+  p.pdl = pdl ? 1u : 0u;
   p.stage_bytes = h_rows * 128u + kSmemB;  // h_rows is a multiple of 8: 1 KB swizzle atoms
   p.n_stages = kRingBytes / p.stage_bytes < uint32_t(kMaxStages) ? kRingBytes / p.stage_bytes
                                                                 : uint32_t(kMaxStages);
@@ -308,8 +322,9 @@ fs_status check_sample(const fs_sample_args* a) {
 namespace fs {
 namespace {
 // fs_sample, optionally also writing the ids to `out_idx_host` (a device
-// address of mapped host memory).
-fs_status sample(const fs_sample_args* a, int64_t* out_idx_host, void* stream_ptr) {
+// address of mapped host memory); with pdl the kernel overlaps the kernel
+// before it on the stream, which writes its H and per-row inputs.
+fs_status sample(const fs_sample_args* a, int64_t* out_idx_host, bool pdl, void* stream_ptr) {
   const fs_status chk = check_sample(a);
   if (chk != FS_OK) return chk;
   const int64_t B = a->B, V = a->V;
@@ -325,7 +340,7 @@ fs_status sample(const fs_sample_args* a, int64_t* out_idx_host, void* stream_pt
                                 static_cast<uint8_t*>(a->workspace) + kKeysOffset)
                           : nullptr;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
-  const fs_status lst = run_stage1(a, a->out_tile_lse ? kModeLse : kModeSample, p, stream);
+  const fs_status lst = run_stage1(a, a->out_tile_lse ? kModeLse : kModeSample, p, stream, pdl);
   if (lst != FS_OK || a->out_lse == nullptr) return lst;
   return launch_row_lse(a->out_tile_lse, a->temperature, B, fs_num_tiles(V), a->out_lse, stream);
 }
@@ -341,11 +356,20 @@ void* mapped_host(const void* host) {
   }
   return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
 }
+
+// Whether W (the one input the overlapped kernel reads before the copy in is
+// complete) lies in the buffer that copy writes.
+bool w_in_buffer(const fs_sample_args* a, const void* buf, size_t bytes) {
+  const uintptr_t w0 = reinterpret_cast<uintptr_t>(a->W);
+  const uintptr_t w1 = w0 + uintptr_t(a->V - 1) * uintptr_t(a->ldw) * 2u + uintptr_t(a->d) * 2u;
+  const uintptr_t b0 = reinterpret_cast<uintptr_t>(buf), b1 = b0 + bytes;
+  return w0 < b1 && b0 < w1;
+}
 }  // namespace
 }  // namespace fs
 
 extern "C" fs_status fs_sample(const fs_sample_args* a, void* stream_ptr) {
-  return sample(a, nullptr, stream_ptr);
+  return sample(a, nullptr, false, stream_ptr);
 }
 
 extern "C" size_t fs_topk_workspace_size(int64_t B, int64_t V, int64_t K) {
@@ -450,9 +474,11 @@ extern "C" fs_status fs_sample_host(const fs_sample_args* a, const void* host_in
   // Inputs in: mapped host memory is read by SMs over the host link (on a
   // Grace host, NVLink-C2C: several times the copy engine's rate for a
   // decode-sized H); other host memory goes through cudaMemcpyAsync.
+  bool overlap = false;  // the sampling kernel overlaps the copy kernel
   if (in_bytes > 0) {
     const void* src = mapped_host(host_in);
     if (src != nullptr) {
+      overlap = !w_in_buffer(a, dev_in, in_bytes);
       const int vec = (reinterpret_cast<uintptr_t>(src) % 16 == 0 &&
                        reinterpret_cast<uintptr_t>(dev_in) % 16 == 0) ? 1 : 0;
       const size_t per_block = 256u * (vec ? 16u : 1u);
@@ -470,7 +496,7 @@ extern "C" fs_status fs_sample_host(const fs_sample_args* a, const void* host_in
   // Ids out: the kernel's last CTA writes them to mapped host memory as well;
   // otherwise they are copied back.
   int64_t* out_mapped = static_cast<int64_t*>(mapped_host(host_out));
-  const fs_status run = sample(a, out_mapped, stream_ptr);
+  const fs_status run = sample(a, out_mapped, overlap, stream_ptr);
   if (run != FS_OK) return run;
   if (out_mapped == nullptr &&
       cudaMemcpyAsync(host_out, a->out_idx, size_t(a->B) * sizeof(int64_t),

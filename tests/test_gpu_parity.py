@@ -74,6 +74,27 @@ def test_ragged_shapes(B, d, V):
     compare(p, dev, seed=3, offset=5, scores=True)
 
 
+def test_strided_inputs():
+    """H and W as column slices of wider buffers (row strides ldh, ldw > d)
+    and a mask with spare words per row: the same results as on contiguous
+    copies, and parity with the oracle."""
+    B, d, V = 40, 96, 3000
+    p = make_problem(B, d, V, T="row-uniform", per_row_seeds=True, mask_frac=0.04, seed=16)
+    Hw = torch.zeros((B, d + 40), dtype=torch.bfloat16, device="cuda")
+    Ww = torch.zeros((V, d + 24), dtype=torch.bfloat16, device="cuda")
+    Mw = torch.zeros((B, p["vocab_mask"].shape[1] + 5), dtype=torch.int32, device="cuda")
+    Hw[:, 8:8 + d] = p["H"]
+    Ww[:, :d] = p["W"]
+    Mw[:, :p["vocab_mask"].shape[1]] = p["vocab_mask"]
+    q = dict(p, H=Hw[:, 8:8 + d], W=Ww[:, :d], vocab_mask=Mw)
+    assert q["H"].stride(0) == d + 40 and q["W"].stride(0) == d + 24
+    a = run_device(p, seed=3, offset=8)
+    b = run_device(q, seed=3, offset=8)
+    for k in a:
+        assert np.array_equal(a[k], b[k]), k
+    compare(p, b, seed=3, offset=8)
+
+
 def test_mixed_rows_seeds_mask():
     """Per-row seeds, per-row temperatures with greedy rows, a vocab mask with
     fully masked tiles and a fully masked row."""
