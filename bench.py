@@ -29,6 +29,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "µs/call and % of HBM/tensor roofline, fused LM-head+sample, d=4096 V=151936"
+L2_BYTES = 129 * 2**20  # GB300 L2
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -409,7 +410,9 @@ def run_ours(args):
         "config": {
             "workload": describe(w, B),
             "B": B, "d": d, "V": V, "global_batch": B * world,
-            "l2": "inputs exceed L2 (W is %.2f GB), no flush" % (V * d * 2 / 1e9),
+            "l2": (("inputs exceed L2 (W is %.2f GB), no flush" % (V * d * 2 / 1e9))
+                   if V * d * 2 > L2_BYTES else
+                   ("W (%.1f MB) fits in L2: warm, no flush" % (V * d * 2 / 1e6))),
             "parallelism": "replicas" if world > 1 else "single-gpu",
         },
         "tokens_per_s": round(B * world / (us_call * 1e-6), 1),
