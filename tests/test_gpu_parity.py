@@ -224,6 +224,38 @@ def test_graph_replay_matches_eager():
         assert np.array_equal(out.cpu().numpy(), eager)
 
 
+def test_host_step_in_a_cuda_graph():
+    """fs_sample_host without its wait, captured in a CUDA graph (copy-in
+    kernel, overlapped sampling kernel writing mapped host memory): each
+    replay picks up new host inputs and delivers their ids to host memory."""
+    B, d, V = 16, 64, 3000
+    p = make_problem(B, d, V, T=1.0, seed=17)
+    hb = p["H"].view(torch.uint8).reshape(-1)
+    host_in = torch.zeros(hb.numel(), dtype=torch.uint8).pin_memory()
+    dev_in = torch.empty_like(host_in, device="cuda")
+    out = torch.empty(B, dtype=torch.int64, device="cuda")
+    ws = torch.zeros(fs.fs_workspace_size(B, V), dtype=torch.uint8, device="cuda")
+    host_out = torch.full((B,), -7, dtype=torch.int64).pin_memory()
+    args = fs.FsSampleArgs(H=dev_in.data_ptr(), W=p["W"].data_ptr(), seed=3, offset=2, B=B, d=d,
+                           V=V, ldh=d, ldw=d, out_idx=out.data_ptr(), workspace=ws.data_ptr(),
+                           workspace_bytes=ws.numel())
+    s = torch.cuda.Stream()
+    host_in.copy_(hb.cpu())
+    fs.fs_sample_host(args, host_in, dev_in, host_out, stream=s)  # sets the device up
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        fs.fs_sample_host(args, host_in, dev_in, host_out, sync=False, stream=s)
+    for k in range(3):
+        H = wl.make_hidden(B, d, seed=900 + k, device="cuda")
+        want = fs.fs_sample(H, p["W"], seed=3, offset=2)
+        torch.cuda.synchronize()
+        host_in.copy_(H.view(torch.uint8).reshape(-1).cpu())
+        host_out.fill_(-7)
+        g.replay()
+        torch.cuda.synchronize()
+        assert np.array_equal(host_out.numpy(), want.cpu().numpy()), k
+
+
 def test_chi_square_on_device():
     """Device draws over many offsets follow softmax(l/T) (Pearson
     chi-square), and equal the oracle's draws offset by offset."""
