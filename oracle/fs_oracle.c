@@ -22,7 +22,7 @@
  *            passages of the aitrends.kr write-up)
  *   sample = lowest v attaining max_v s            (Stage 2, "Reduction")
  *
- * Readings where the pages are silent (each is listed in the design doc):
+ * Readings where the pages are silent (the choices this oracle makes):
  *   - the uniform u comes from Philox4x32-10 (Salmon, Moraes, Dror, Shaw,
  *     "Parallel Random Numbers: As Easy as 1, 2, 3", SC'11) with
  *     key = (seed_b & 0xffffffff, seed_b >> 32),
@@ -276,7 +276,7 @@ int fso_sample_rows(const uint16_t *H, const uint16_t *W, int64_t B, int64_t d,
   return 0;
 }
 
-/* Threads an OpenMP parallel region of this build uses (1 without OpenMP),
+/* Threads an OpenMP parallel region of this library uses (1 without OpenMP),
  * and a setter for it (timing only; the results do not depend on it). */
 #ifdef _OPENMP
 #include <omp.h>
