@@ -268,6 +268,16 @@ fs_status fs_gumbel_noise(const uint64_t *seeds, uint64_t seed, uint64_t offset,
                           float *out, void *stream);
 
 /*
+ * Diagnostic: the transform from one 32-bit Philox output word to the Gumbel
+ * noise g the stage-1 kernel uses (the word's low 23 bits give
+ * u = (k + 1/2) 2^-23, then g = -log(-log u)), applied to n given words
+ * (device uint32 [n]) into out (device fp32 [n]) -- the same device code as
+ * fs_sample, so every uniform level can be checked.  FS_ERR_INVALID_ARG for
+ * n < 0 or null buffers with n > 0.
+ */
+fs_status fs_gumbel_transform(const uint32_t *words, int64_t n, float *out, void *stream);
+
+/*
  * Diagnostic: run the sampling kernels' bounded wait on a barrier that nothing
  * ever arrives on, giving up after limit_ns (1e3 <= limit_ns <= 1e9).  The
  * kernel records the timeout in the device error word and returns, exactly as

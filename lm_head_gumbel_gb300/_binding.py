@@ -76,6 +76,8 @@ def load_library(path: str = LIB_PATH):
     lib.fs_gumbel_noise.argtypes = [_c_ptr, _c_u64, _c_u64, _c_i64, _c_i64, _c_i64, _c_i64,
                                     _c_ptr, _c_ptr]
     lib.fs_gumbel_noise.restype = ctypes.c_int
+    lib.fs_gumbel_transform.argtypes = [_c_ptr, _c_i64, _c_ptr, _c_ptr]
+    lib.fs_gumbel_transform.restype = ctypes.c_int
     lib.fs_topk_workspace_size.argtypes = [_c_i64, _c_i64, _c_i64]
     lib.fs_topk_workspace_size.restype = ctypes.c_size_t
     lib.fs_sample_topk.argtypes = [ctypes.POINTER(FsSampleArgs), _c_i64, _c_ptr, _c_ptr, _c_ptr]
@@ -300,6 +302,23 @@ def fs_online_merge(state_z, state_L, new_z, new_L, step, *, seeds=None, seed=0,
                                  int(offset) & (2**64 - 1), _stream_handle(stream, dev))
     if st != FS_OK:
         raise FsError(st, "fs_online_merge")
+
+
+def fs_gumbel_transform(words, out=None, stream=None):
+    """The fp32 Gumbel noise of given 32-bit Philox words (an int32 CUDA
+    tensor holding the bit patterns) -- the transform fs_sample applies
+    (diagnostic)."""
+    lib = load_library()
+    if words.dtype != torch.int32 or not words.is_cuda or not words.is_contiguous():
+        raise FsError(FS_ERR_INVALID_ARG, "words must be a contiguous int32 CUDA tensor")
+    if out is None:
+        out = torch.empty(words.shape, dtype=torch.float32, device=words.device)
+    with torch.cuda.device(words.device):
+        st = lib.fs_gumbel_transform(_ptr(words), int(words.numel()), _ptr(out),
+                                     _stream_handle(stream, words.device))
+    if st != FS_OK:
+        raise FsError(st, "fs_gumbel_transform")
+    return out
 
 
 def fs_gumbel_noise(b0, nb, v0, nv, *, seed=0, offset=0, seeds=None, out=None, device=None,

@@ -939,6 +939,13 @@ __global__ void stage_in_kernel(const uint8_t* __restrict__ src, uint8_t* __rest
   }
 }
 
+// The word -> Gumbel transform alone, on given words (diagnostic entry point).
+__global__ void gumbel_transform_kernel(const uint32_t* __restrict__ words, int64_t n,
+                                        float* __restrict__ out) {
+  const int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i < n) out[i] = gumbel_from_word(words[i]);
+}
+
 // The noise stage 1 adds, element by element (diagnostic entry point).
 __global__ void noise_kernel(const uint64_t* __restrict__ seeds, uint64_t seed, uint64_t offset,
                              int64_t b0, int64_t nb, int64_t v0, int64_t nv,

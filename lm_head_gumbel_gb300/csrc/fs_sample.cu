@@ -511,6 +511,21 @@ extern "C" fs_status fs_sample_host(const fs_sample_args* a, const void* host_in
   return FS_OK;
 }
 
+extern "C" fs_status fs_gumbel_transform(const uint32_t* words, int64_t n, float* out,
+                                         void* stream_ptr) {
+  if (n < 0 || (n > 0 && (!words || !out))) return FS_ERR_INVALID_ARG;
+  if (n == 0) return FS_OK;
+  int num_sms = 0;
+  const fs_status st = device_setup(&num_sms);
+  if (st != FS_OK) return st;
+  const int threads = 256;
+  const int64_t blocks = (n + threads - 1) / threads;
+  if (blocks > int64_t(0x7FFFFFFF)) return FS_ERR_INVALID_ARG;
+  gumbel_transform_kernel<<<unsigned(blocks), threads, 0, static_cast<cudaStream_t>(stream_ptr)>>>(
+      words, n, out);
+  return cudaGetLastError() == cudaSuccess ? FS_OK : FS_ERR_CUDA;
+}
+
 extern "C" fs_status fs_gumbel_noise(const uint64_t* seeds, uint64_t seed, uint64_t offset,
                                      int64_t b0, int64_t nb, int64_t v0, int64_t nv, float* out,
                                      void* stream_ptr) {

@@ -107,6 +107,13 @@ def test_null_args_rejected(lib):
     assert lib.fs_sample(None, None) == 1
 
 
+def test_transform_bad_arguments(lib):
+    assert lib.fs_gumbel_transform(None, 5, ctypes.c_void_p(0x1000), None) == 1
+    assert lib.fs_gumbel_transform(ctypes.c_void_p(0x1000), -1, ctypes.c_void_p(0x1000),
+                                   None) == 1
+    assert lib.fs_gumbel_transform(None, 0, None, None) == 0  # nothing to do
+
+
 def test_noise_bad_arguments(lib):
     assert lib.fs_gumbel_noise(None, 0, 0, 0, 1, 0, 1, None, None) == 1
     assert lib.fs_gumbel_noise(None, 0, 0, -1, 1, 0, 1, ctypes.c_void_p(0x1000), None) == 1

@@ -40,9 +40,24 @@ def test_noise_matches_oracle():
         assert err.max() < 2e-5, err.max()
 
 
+def test_noise_transform_every_uniform_level():
+    """Exhaustive: the device's word -> Gumbel transform for every one of the
+    2^23 uniform levels u = (k + 1/2) 2^-23 (only a word's low 23 bits count)
+    is within 1e-5 of g = -log(-log u) in fp64, and the high 9 bits are
+    ignored."""
+    k = torch.arange(1 << 23, dtype=torch.int64)
+    g = fs.fs_gumbel_transform(k.to(torch.int32).cuda()).cpu().numpy().astype(np.float64)
+    u = (k.numpy().astype(np.float64) + 0.5) * 2.0 ** -23
+    want = -np.log(-np.log(u))
+    err = np.abs(g - want)
+    assert err.max() < 1e-5, (err.max(), int(err.argmax()))
+    hi = (k[:4096] | (0x5A5 << 23)).to(torch.int32).cuda()  # other high bits, same level
+    assert np.array_equal(fs.fs_gumbel_transform(hi).cpu().numpy(), g[:4096].astype(np.float32))
+
+
 def test_noise_accuracy_over_all_uniforms():
-    """The fp32 noise is within 1e-5 of the fp64 value for every one of the
-    2^23 uniform levels (vocabulary ids cover all words of many blocks)."""
+    """Noise from Philox words over 2^21 consecutive vocabulary ids (many
+    Philox blocks) against the oracle's fp64 chain on a subsample."""
     o = oracle.default()
     g = fs.fs_gumbel_noise(0, 1, 0, 1 << 21, seed=42, offset=1).cpu().numpy().ravel()
     sub = np.arange(0, 1 << 21, 997)
