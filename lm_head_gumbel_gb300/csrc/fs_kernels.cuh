@@ -515,7 +515,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n_units = ((p.V + kBlockN - 1) / kBlockN) * p.n_mt;
+  // Vocabulary blocks from the tile count: V + 255 overflows 32 bits near V = 2^31.
+  const int n_units = ((p.n_tiles + 1) / 2) * p.n_mt;
 
   if (threadIdx.x == 0) {
     for (uint32_t s = 0; s < p.n_stages; ++s) {
@@ -729,7 +730,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int pair_id = int(blockIdx.x) >> 1;
   const int n_pairs = int(gridDim.x) >> 1;
   const int n_mp = (p.B + 2 * kBlockM - 1) / (2 * kBlockM);
-  const int n_units = ((p.V + kBlockN - 1) / kBlockN) * n_mp;
+  const int n_units = ((p.n_tiles + 1) / 2) * n_mp;  // not from V + 255 (32-bit overflow)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kPairStages; ++s) {

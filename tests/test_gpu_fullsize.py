@@ -136,3 +136,45 @@ def test_large_vocab_head_partition_merge(B):
         parts = [merge.lse_merge(dev["tile_lse"][b, bounds[k]:bounds[k + 1]]) for k in range(4)]
         whole = merge.lse_merge(ref["tile_lse"][r])
         assert abs(merge.lse_merge(parts) - whole) < 2e-3
+
+
+def test_largest_batch():
+    """B = 65535, the largest batch the ABI takes (CTA pairs, 256 pair blocks),
+    on a ragged vocabulary: sampled rows against the oracle and the
+    whole-batch properties."""
+    B, d, V = 65535, 64, 520
+    p = make_problem(B, d, V, T="row-uniform", per_row_seeds=True, seed=93)
+    dev = run_device(p, seed=8, offset=4, lse=False)
+    whole_batch_properties(p, dev, V)
+    compare(p, dev, [0, 1, 255, 256, 12345, 65279, 65534], seed=8, offset=4)
+
+
+def test_largest_vocabulary():
+    """V = 2^31 - 1, the largest vocabulary the ABI takes (a 32 GiB W at
+    d = 8): the first, a middle and the last (partial) tile against the
+    oracle's logits and noise at those global ids, ids near 2^31 through the
+    packed row keys, and the sample = the best tile's argmax."""
+    import oracle
+    from oracle import parity
+    V, d, B, T = 2**31 - 1, 8, 2, 1.0
+    _W_CACHE.clear()
+    torch.cuda.empty_cache()
+    W = wl.make_weights(d, V, seed=91, device="cuda")
+    p = make_problem(B, d, V, T=T, seed=92, W=W)
+    dev = run_device(p, seed=5, offset=3, lse=False)
+    nt = dev["tile_max"].shape[1]
+    assert nt == (V + 127) // 128
+    whole_batch_properties(p, dev, V)
+    o = oracle.default()
+    Hb = wl.bf16_bits(p["H"])
+    for t in (0, nt // 2, nt - 1):
+        v0, v1 = t * 128, min(V, t * 128 + 128)
+        s = o.logits(Hb, wl.bf16_bits(W[v0:v1])) / T + o.noise_grid(0, B, v0, v1 - v0, seed=5,
+                                                                     offset=3)
+        for b in range(B):
+            order = np.argsort(-s[b], kind="stable")
+            assert abs(dev["tile_max"][b, t] - s[b, order[0]]) < parity.TOL_MAX, (b, t)
+            if s[b, order[0]] - s[b, order[1]] > parity.GAP:
+                assert dev["tile_idx"][b, t] == v0 + order[0], (b, t)
+    del W, p, dev
+    torch.cuda.empty_cache()
