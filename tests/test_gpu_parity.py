@@ -79,6 +79,7 @@ def test_tiny(T):
     (1, 8, 1), (1, 8, 2), (3, 72, 100), (1, 264, 1000), (5, 64, 129), (2, 136, 4097),
     (7, 200, 255), (33, 96, 257), (129, 64, 640), (130, 128, 3000), (300, 64, 1100),
     (256, 72, 100), (256, 64, 1), (260, 64, 300), (512, 40, 700), (511, 64, 1300),
+    (4, 16384, 3000), (130, 8200, 700),  # long K loops (256 and 129 slices)
 ])
 def test_ragged_shapes(B, d, V):
     """Odd B (several 128-row blocks, CTA pairs for even block counts), d not
