@@ -171,6 +171,46 @@ def test_rows_do_not_depend_on_the_batch(V):
     assert np.array_equal(runs[384]["tile_max"][:256], runs[256]["tile_max"])
 
 
+def test_tiny_temperature_is_effectively_greedy():
+    """T = 1e-4 (l/T ~ 1e5, far from fp32 overflow): the sample is the argmax
+    of the logits wherever the logit gap is clearly wider than the noise's
+    reach, and equals the oracle's id wherever its score gap exceeds 1 (the
+    fp32 logit error, ~1e-5, is magnified 1e4 times in the score)."""
+    B, d, V = 16, 64, 2000
+    p = make_problem(B, d, V, T=1e-4, seed=18)
+    dev = run_device(p, seed=4, offset=1, lse=False, tiles=False)
+    o = oracle.default()
+    Hb, Wb = wl.bf16_bits(p["H"]), wl.bf16_bits(p["W"])
+    ref = o.sample(Hb, Wb, temperature=p["temperature"].cpu().numpy(), seed=4, offset=1)
+    gated = ref["gap"] > 1.0
+    assert gated.sum() >= B // 2 and np.array_equal(dev["idx"][gated], ref["idx"][gated])
+    logits = o.logits(Hb, Wb)
+    top2 = np.sort(logits, axis=1)[:, -2:]
+    clear = (top2[:, 1] - top2[:, 0]) > 40 * 1e-4  # noise spans about 20 nats at most
+    assert np.array_equal(dev["idx"][clear], logits.argmax(axis=1)[clear])
+
+
+def test_nan_logits_are_never_sampled():
+    """W rows of NaN (so their logits are NaN in every row) are excluded like
+    masked ids; a tile made only of them reports (-inf, -1)."""
+    B, d, V = 8, 64, 700
+    p = make_problem(B, d, V, T=1.0, seed=19)
+    W = p["W"].clone()
+    nan_ids = [3, 130, 131, 600]
+    W[nan_ids] = float("nan")
+    W[256:384] = float("nan")  # all of tile 2
+    q = dict(p, W=W)
+    for off in range(20):
+        dev = run_device(q, seed=2, offset=off, lse=False)
+        assert not np.isin(dev["idx"], nan_ids + list(range(256, 384))).any()
+        assert np.all(dev["tile_idx"][:, 2] == -1) and np.all(np.isneginf(dev["tile_max"][:, 2]))
+    o = oracle.default()
+    ref = o.sample(wl.bf16_bits(p["H"]), wl.bf16_bits(W), temperature=p["temperature"].cpu().numpy(),
+                   seed=2, offset=19)
+    gated = ref["gap"] > parity.GAP
+    assert np.array_equal(dev["idx"][gated], ref["idx"][gated])
+
+
 def test_host_step_matches_device_call():
     """fs_sample_host (host inputs -> device -> sampled ids back in host
     memory, one call) gives what fs_sample gives on the same inputs, with and
