@@ -259,6 +259,41 @@ def test_host_step_matches_device_call():
     assert torch.equal(dev_in2[1:host_in.numel() + 1].cpu(), host_in)
 
 
+def test_concurrent_host_threads():
+    """Four host threads, each with its own stream and workspace, sampling the
+    same problems at once give exactly the single-thread results."""
+    import threading
+    p = make_problem(24, 96, 3000, T="row-uniform", per_row_seeds=True, seed=20)
+    want = {off: run_device(p, seed=9, offset=off, lse=False, tiles=False)["idx"]
+            for off in range(8)}
+    errors = []
+
+    def worker(tid):
+        try:
+            s = torch.cuda.Stream()
+            ws = torch.zeros(fs.fs_workspace_size(24, 3000), dtype=torch.uint8, device="cuda")
+            out = torch.empty((8, 24), dtype=torch.int64, device="cuda")
+            with torch.cuda.stream(s):
+                for rep in range(10):
+                    for off in range(8):
+                        fs.fs_sample(p["H"], p["W"], temperature=p["temperature"],
+                                     seeds=p["seeds"], seed=9, offset=off, out_idx=out[off],
+                                     workspace=ws, stream=s)
+            s.synchronize()
+            for off in range(8):
+                if not np.array_equal(out[off].cpu().numpy(), want[off]):
+                    errors.append((tid, off))
+        except Exception as e:  # reported below
+            errors.append((tid, repr(e)))
+
+    threads = [threading.Thread(target=worker, args=(t,)) for t in range(4)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+
+
 def test_graph_replay_matches_eager():
     p = make_problem(8, 64, 3000, T=1.0, seed=8)
     eager = run_device(p, offset=4)["idx"]
