@@ -373,8 +373,8 @@ def run_ours(args):
 
     def e2e_step(k):
         args_c.offset = k
-        # sync=1: the sampled ids feed the next decode step
-        if lib.fs_sample_host(args_ref, hp, dp, n_in, op, 1, sh) != fs.FS_OK:
+        # wait for the ids: they feed the next decode step
+        if lib.fs_sample_host(args_ref, hp, dp, n_in, op, fs.FS_SYNC_IDS, sh) != fs.FS_OK:
             raise SystemExit("fs_sample_host failed")
 
     for k in range(3):

@@ -169,6 +169,12 @@ fs_status fs_sample(const fs_sample_args *args, void *stream);
  */
 fs_status fs_sample_noalloc(const fs_sample_args *args, void *stream);
 
+/* Waits of fs_sample_host. */
+#define FS_SYNC_NONE 0   /* return once the work is enqueued                          */
+#define FS_SYNC_STREAM 1 /* return after the stream has finished                      */
+#define FS_SYNC_IDS 2    /* return as soon as all ids are in host_out (the kernel may  */
+                         /* still be winding down; later work on the stream follows it) */
+
 /*
  * One decode step from host memory: the end-to-end form of fs_sample, in one
  * call.  Enqueues on `stream`, in order: a copy of in_bytes from host_in (host
@@ -176,12 +182,16 @@ fs_status fs_sample_noalloc(const fs_sample_args *args, void *stream);
  * the fs_sample call described by args -- whose input pointers the caller has
  * pointed into dev_in, or anywhere else on the device -- and a copy of the B
  * sampled ids from args->out_idx (required) to host_out (host int64 [B],
- * pinned).  With sync != 0 it then waits for the stream, so the ids are in
- * host_out when it returns FS_OK.  in_bytes may be 0 (inputs already on the
- * device).  Errors: FS_ERR_INVALID_ARG for a null args, args->out_idx or
- * host_out, or a null host_in / dev_in with in_bytes > 0; every error of
- * fs_sample's argument checks -- both before anything is enqueued; FS_ERR_CUDA
- * for a failed copy, launch or wait.
+ * pinned).  `sync` is one of FS_SYNC_*: FS_SYNC_STREAM waits for the stream;
+ * FS_SYNC_IDS, when host_out is page-locked (the kernel then writes the ids
+ * into it directly), watches host_out until every id has arrived, which
+ * returns a few microseconds earlier than a stream wait (otherwise it waits
+ * for the stream); FS_SYNC_NONE returns at once.  in_bytes may be 0 (inputs
+ * already on the device).  Errors: FS_ERR_INVALID_ARG for a null args,
+ * args->out_idx or host_out, a null host_in / dev_in with in_bytes > 0, or an
+ * unknown sync; every error of fs_sample's argument checks -- all before
+ * anything is enqueued; FS_ERR_CUDA for a failed copy, launch or wait (a watch
+ * gives up after 10 s and reports the stream's status).
  */
 fs_status fs_sample_host(const fs_sample_args *args, const void *host_in, void *dev_in,
                          size_t in_bytes, int64_t *host_out, int sync, void *stream);

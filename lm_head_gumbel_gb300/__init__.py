@@ -6,7 +6,8 @@ tests and the benchmark.
 """
 from ._binding import (FS_ERR_CUDA, FS_ERR_DEVICE_TIMEOUT, FS_ERR_INVALID_ARG,  # noqa: F401
                        FS_ERR_UNSUPPORTED, FS_ERR_WORKSPACE, FS_MERGE_EXACT,
-                       FS_MERGE_GROUP_GUMBEL, FS_OK, FS_TILE, FS_TOPK_MAX, LIB_PATH, FsError,
+                       FS_MERGE_GROUP_GUMBEL, FS_OK, FS_SYNC_IDS, FS_SYNC_NONE, FS_SYNC_STREAM,
+                       FS_TILE, FS_TOPK_MAX, LIB_PATH, FsError,
                        FsSampleArgs, fs_group_merge, fs_gumbel_noise, fs_gumbel_transform,
                        fs_last_device_error,
                        fs_online_merge, fs_sample_topk, fs_topk_workspace_size,

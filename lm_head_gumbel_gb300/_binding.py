@@ -22,6 +22,7 @@ FS_ERR_CUDA = 3
 FS_ERR_DEVICE_TIMEOUT = 4
 FS_ERR_WORKSPACE = 5
 FS_TOPK_MAX = 16
+FS_SYNC_NONE, FS_SYNC_STREAM, FS_SYNC_IDS = 0, 1, 2
 FS_MERGE_EXACT = 0
 FS_MERGE_GROUP_GUMBEL = 1
 
@@ -207,9 +208,11 @@ def fs_sample_host(args, host_in, dev_in, host_out, *, sync=True, stream=None, d
     copy host_in (pinned uint8 host tensor) to dev_in (uint8 device tensor of
     at least the same size), run fs_sample with ``args`` (an FsSampleArgs
     whose input pointers point into dev_in, or elsewhere on the device), copy
-    the B sampled ids to host_out (pinned int64 [B] host tensor) and, with
-    ``sync``, wait for them.  host_in may be None (nothing to copy).  Pass
-    ``args`` by reference (``ctypes.byref``) to reuse one argument block."""
+    the B sampled ids to host_out (pinned int64 [B] host tensor) and wait:
+    ``sync`` is True / FS_SYNC_STREAM (the stream), FS_SYNC_IDS (until the
+    ids are in host_out) or False / FS_SYNC_NONE.  host_in may be None
+    (nothing to copy).  Pass ``args`` by reference (``ctypes.byref``) to
+    reuse one argument block."""
     lib = load_library()
     device = torch.device(device or "cuda")
     n = 0 if host_in is None else host_in.numel() * host_in.element_size()
@@ -221,7 +224,7 @@ def fs_sample_host(args, host_in, dev_in, host_out, *, sync=True, stream=None, d
     ref = args if isinstance(args, type(ctypes.byref(FsSampleArgs()))) else ctypes.byref(args)
     with torch.cuda.device(device):
         st = lib.fs_sample_host(ref, _ptr(host_in), _ptr(dev_in) if host_in is not None else None,
-                                n, _ptr(host_out), 1 if sync else 0,
+                                n, _ptr(host_out), int(sync),
                                 _stream_handle(stream, device))
     if st != FS_OK:
         raise FsError(st, "fs_sample_host")

@@ -6,6 +6,9 @@
 
 #include <cmath>
 #include <cstdint>
+#include <atomic>
+#include <chrono>
+#include <climits>
 #include <mutex>
 
 #include "fs_kernels.cuh"
@@ -357,6 +360,27 @@ void* mapped_host(const void* host) {
   return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
 }
 
+constexpr int64_t kIdPending = INT64_MIN;
+
+// Wait until every entry of the mapped host buffer `ids` has been written by
+// the kernel (none is kIdPending any more).  Bounded: after 10 s of waiting,
+// or if the stream reports an error, the stream's own status decides.
+fs_status watch_ids(const int64_t* ids, int64_t n, cudaStream_t stream) {
+  const volatile int64_t* v = ids;
+  const auto t0 = std::chrono::steady_clock::now();
+  for (int64_t b = 0; b < n; ++b) {
+    while (v[b] == kIdPending) {
+      if (std::chrono::steady_clock::now() - t0 > std::chrono::seconds(10)) {
+        const cudaError_t e = cudaStreamSynchronize(stream);
+        cudaGetLastError();
+        return e == cudaSuccess && v[b] != kIdPending ? FS_OK : FS_ERR_CUDA;
+      }
+    }
+  }
+  std::atomic_thread_fence(std::memory_order_acquire);
+  return FS_OK;
+}
+
 // Whether W (the one input the overlapped kernel reads before the copy in is
 // complete) lies in the buffer that copy writes.
 bool w_in_buffer(const fs_sample_args* a, const void* buf, size_t bytes) {
@@ -464,6 +488,8 @@ extern "C" fs_status fs_sample_host(const fs_sample_args* a, const void* host_in
                                     size_t in_bytes, int64_t* host_out, int sync,
                                     void* stream_ptr) {
   if (a == nullptr || host_out == nullptr || a->out_idx == nullptr) return FS_ERR_INVALID_ARG;
+  if (sync != FS_SYNC_NONE && sync != FS_SYNC_STREAM && sync != FS_SYNC_IDS)
+    return FS_ERR_INVALID_ARG;
   if (in_bytes > 0 && (host_in == nullptr || dev_in == nullptr)) return FS_ERR_INVALID_ARG;
   const fs_status chk = check_sample(a);
   if (chk != FS_OK) return chk;
@@ -496,6 +522,10 @@ extern "C" fs_status fs_sample_host(const fs_sample_args* a, const void* host_in
   // Ids out: the kernel's last CTA writes them to mapped host memory as well;
   // otherwise they are copied back.
   int64_t* out_mapped = static_cast<int64_t*>(mapped_host(host_out));
+  const bool watch = sync == FS_SYNC_IDS && out_mapped != nullptr;
+  if (watch) {  // no id is ever this value, so each entry shows when it lands
+    for (int64_t b = 0; b < a->B; ++b) host_out[b] = kIdPending;
+  }
   const fs_status run = sample(a, out_mapped, overlap, stream_ptr);
   if (run != FS_OK) return run;
   if (out_mapped == nullptr &&
@@ -504,6 +534,7 @@ extern "C" fs_status fs_sample_host(const fs_sample_args* a, const void* host_in
     cudaGetLastError();
     return FS_ERR_CUDA;
   }
+  if (watch) return watch_ids(host_out, a->B, stream);
   if (sync && cudaStreamSynchronize(stream) != cudaSuccess) {
     cudaGetLastError();
     return FS_ERR_CUDA;

@@ -184,3 +184,5 @@ def test_host_step_bad_arguments(lib):
     assert f(ctypes.byref(_args(**ws)), hin, None, 64, hout, 1, None) == 1         # no dev_in
     assert f(ctypes.byref(_args(**dict(ws, B=0))), hin, din, 64, hout, 1, None) == 1
     assert f(ctypes.byref(_args(**dict(ws, workspace=None))), hin, din, 64, hout, 1, None) == 5
+    assert f(ctypes.byref(_args(**ws)), hin, din, 64, hout, 3, None) == 1          # bad sync
+    assert f(ctypes.byref(_args(**ws)), hin, din, 64, hout, -1, None) == 1

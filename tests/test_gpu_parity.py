@@ -245,6 +245,11 @@ def test_host_step_matches_device_call():
     host_out.fill_(-7)
     fs.fs_sample_host(args, None, None, host_out)  # inputs already on the device
     assert np.array_equal(host_out.numpy(), want)
+    for _ in range(3):  # waiting on the ids themselves
+        host_out.fill_(-7)
+        fs.fs_sample_host(args, host_in, dev_in, host_out, sync=fs.FS_SYNC_IDS)
+        assert np.array_equal(host_out.numpy(), want)
+    torch.cuda.synchronize()
     # pageable (unmapped) host buffers take the copy-engine path
     dev_in.zero_()
     paged_out = torch.full((B,), -7, dtype=torch.int64)
