@@ -138,6 +138,30 @@ def test_large_vocab_head_partition_merge(B):
         assert abs(merge.lse_merge(parts) - whole) < 2e-3
 
 
+def test_stage1_only_call_at_full_size():
+    """out_idx = NULL: only the per-tile (max, argmax, LSE) are written (the
+    per-partition summaries a caller merges itself); they equal those of the
+    full call, and their exact merge is its sample."""
+    W, Wb = weights("qwen3-8b")
+    B = 64
+    p = make_problem(B, W.shape[1], W.shape[0], T="row-uniform", per_row_seeds=True, seed=94, W=W)
+    full = run_device(p, seed=3, offset=6, lse=True)
+    nt = full["tile_max"].shape[1]
+    tm = torch.empty((B, nt), dtype=torch.float32, device="cuda")
+    ti = torch.empty((B, nt), dtype=torch.int32, device="cuda")
+    tl = torch.empty((B, nt), dtype=torch.float32, device="cuda")
+    assert fs.fs_sample(p["H"], W, temperature=p["temperature"], seeds=p["seeds"], seed=3,
+                        offset=6, out_tile_max=tm, out_tile_idx=ti, out_tile_lse=tl,
+                        reduce=False) is None
+    torch.cuda.synchronize()
+    assert np.array_equal(tm.cpu().numpy(), full["tile_max"])
+    assert np.array_equal(ti.cpu().numpy(), full["tile_idx"])
+    assert np.array_equal(tl.cpu().numpy(), full["tile_lse"])
+    for b in range(B):
+        i, _ = merge.partition_argmax(full["tile_max"][b], full["tile_idx"][b], [0, nt])
+        assert i == full["idx"][b]
+
+
 def test_largest_batch():
     """B = 65535, the largest batch the ABI takes (CTA pairs, 256 pair blocks),
     on a ragged vocabulary: sampled rows against the oracle and the

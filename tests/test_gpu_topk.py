@@ -119,6 +119,32 @@ def test_topk_pairs_follow_plackett_luce():
     assert pval > 1e-3, pval
 
 
+def test_topk_on_a_vocabulary_shard():
+    """K draws on a shard W[v0:v1] sampled with vocab_offset = v0 return
+    global ids, and are the K best of the full row's scores restricted to
+    the shard (the oracle's scores of the whole vocabulary, sliced)."""
+    B, d, V, K, v0, v1 = 12, 64, 4096, 8, 1024, 3072
+    p = make_problem(B, d, V, T="row-uniform", per_row_seeds=True, seed=61)
+    out = torch.empty((B, K), dtype=torch.int64, device="cuda")
+    score = torch.empty((B, K), dtype=torch.float32, device="cuda")
+    fs.fs_sample_topk(p["H"], p["W"][v0:v1], K, temperature=p["temperature"], seeds=p["seeds"],
+                      seed=7, offset=5, vocab_offset=v0, out_topk_idx=out, out_topk_score=score)
+    torch.cuda.synchronize()
+    idx, sc = out.cpu().numpy(), score.cpu().numpy()
+    assert np.all((idx >= v0) & (idx < v1))
+    o = oracle.default()
+    ref = o.sample(wl.bf16_bits(p["H"]), wl.bf16_bits(p["W"]),
+                   temperature=p["temperature"].cpu().numpy(), seeds=wl.u64_bits(p["seeds"]),
+                   seed=7, offset=5, want_scores=True)
+    ridx, rval = oracle.topk_from_scores(ref["scores"][:, v0:v1], K + 1)
+    for b in range(B):
+        gaps = -np.diff(rval[b])
+        for j in range(K):
+            assert abs(sc[b, j] - rval[b, j]) <= parity.TOL_MAX, (b, j)
+            if (j == 0 or gaps[j - 1] > parity.GAP) and gaps[j] > parity.GAP:
+                assert idx[b, j] == v0 + ridx[b, j], (b, j)
+
+
 @pytest.mark.parametrize("B,V", [(384, 5000), (512, 3000), (136, 40000)])
 def test_topk_rows_changing_between_units(B, V):
     """Batches whose epilogue threads change rows from unit to unit (three
