@@ -184,9 +184,10 @@ fs_status fs_sample_noalloc(const fs_sample_args *args, void *stream);
  * sampled ids from args->out_idx (required) to host_out (host int64 [B],
  * pinned).  `sync` is one of FS_SYNC_*: FS_SYNC_STREAM waits for the stream;
  * FS_SYNC_IDS, when host_out is page-locked (the kernel then writes the ids
- * into it directly), watches host_out until every id has arrived, which
- * returns a few microseconds earlier than a stream wait (otherwise it waits
- * for the stream); FS_SYNC_NONE returns at once.  in_bytes may be 0 (inputs
+ * into it directly) and the stream had no pending work at the call (so no
+ * earlier call can still write host_out), watches host_out until every id
+ * has arrived, a few microseconds sooner than a stream wait (otherwise it
+ * waits for the stream); FS_SYNC_NONE returns at once.  in_bytes may be 0 (inputs
  * already on the device).  Errors: FS_ERR_INVALID_ARG for a null args,
  * args->out_idx or host_out, a null host_in / dev_in with in_bytes > 0, or an
  * unknown sync; every error of fs_sample's argument checks -- all before

@@ -497,6 +497,26 @@ extern "C" fs_status fs_sample_host(const fs_sample_args* a, const void* host_in
   const fs_status st = device_setup(&num_sms);
   if (st != FS_OK) return st;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  // Ids out: the kernel's last CTA writes them to mapped host memory as well;
+  // otherwise they are copied back.  Watching host_out for them is safe only
+  // if nothing enqueued earlier on the stream (an earlier call that did not
+  // wait) can still write it; otherwise the call waits for the stream.
+  int64_t* out_mapped = static_cast<int64_t*>(mapped_host(host_out));
+  bool watch = sync == FS_SYNC_IDS && out_mapped != nullptr;
+  if (watch) {
+    const cudaError_t q = cudaStreamQuery(stream);
+    if (q != cudaSuccess) {
+      if (q != cudaErrorNotReady) {
+        cudaGetLastError();
+        return FS_ERR_CUDA;
+      }
+      cudaGetLastError();
+      watch = false;
+    }
+  }
+  if (watch) {  // no id is ever this value, so each entry shows when it lands
+    for (int64_t b = 0; b < a->B; ++b) host_out[b] = kIdPending;
+  }
   // Inputs in: mapped host memory is read by SMs over the host link (on a
   // Grace host, NVLink-C2C: several times the copy engine's rate for a
   // decode-sized H); other host memory goes through cudaMemcpyAsync.
@@ -518,13 +538,6 @@ extern "C" fs_status fs_sample_host(const fs_sample_args* a, const void* host_in
       cudaGetLastError();
       return FS_ERR_CUDA;
     }
-  }
-  // Ids out: the kernel's last CTA writes them to mapped host memory as well;
-  // otherwise they are copied back.
-  int64_t* out_mapped = static_cast<int64_t*>(mapped_host(host_out));
-  const bool watch = sync == FS_SYNC_IDS && out_mapped != nullptr;
-  if (watch) {  // no id is ever this value, so each entry shows when it lands
-    for (int64_t b = 0; b < a->B; ++b) host_out[b] = kIdPending;
   }
   const fs_status run = sample(a, out_mapped, overlap, stream_ptr);
   if (run != FS_OK) return run;

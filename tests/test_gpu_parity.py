@@ -250,6 +250,18 @@ def test_host_step_matches_device_call():
         fs.fs_sample_host(args, host_in, dev_in, host_out, sync=fs.FS_SYNC_IDS)
         assert np.array_equal(host_out.numpy(), want)
     torch.cuda.synchronize()
+    # an earlier call that did not wait still writes host_out: the waiting
+    # call must not take that call's ids for its own
+    other = run_device(p, seed=5, offset=22, lse=False, tiles=False)["idx"]
+    assert not np.array_equal(other, want)
+    s2 = torch.cuda.Stream()
+    for _ in range(5):
+        args.offset = 22
+        fs.fs_sample_host(args, host_in, dev_in, host_out, sync=fs.FS_SYNC_NONE, stream=s2)
+        args.offset = 21
+        fs.fs_sample_host(args, host_in, dev_in, host_out, sync=fs.FS_SYNC_IDS, stream=s2)
+        assert np.array_equal(host_out.numpy(), want)
+    torch.cuda.synchronize()
     # pageable (unmapped) host buffers take the copy-engine path
     dev_in.zero_()
     paged_out = torch.full((B,), -7, dtype=torch.int64)
