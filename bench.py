@@ -46,6 +46,13 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU budget of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--library-gemm", action="store_true",
+                    help="also time a library bf16 GEMM (torch.matmul) of the same contraction, "
+                         "logits written out and no sampling, beside the fused call")
+    ap.add_argument("--library-gemm-batches", default="64,256,512")
+    ap.add_argument("--sustain", type=float, default=0.0,
+                    help="with --library-gemm: also run each for this many seconds back to "
+                         "back and report clock, power and energy per call")
     return ap.parse_args()
 
 
@@ -430,6 +437,10 @@ def run_ours(args):
         "sweep": sweep,
         "extensions": extensions,
     }
+    if world == 1 and args.library_gemm:
+        batches = [int(x) for x in args.library_gemm_batches.split(",") if x]
+        line["library_gemm"] = library_gemm_leg(w, inp["W"], dev, stream, batches,
+                                                args.sweep_steps, args.sustain)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inp, B, args.cpu_seconds)
     if rank == 0:
@@ -475,6 +486,75 @@ def describe(w, B):
         parts.append("tile max/argmax/LSE written")
     parts.append("offset=step")
     return ", ".join(parts)
+
+
+def library_gemm_leg(w, W, dev, stream, batches, steps, sustain_s):
+    """Context for the tensor-bound points: the same contraction H W^T as one
+    library bf16 GEMM (torch.matmul, cuBLAS), logits written to HBM and nothing
+    sampled, timed beside the fused sampling call on the same inputs.  Burst:
+    ``steps`` calls after warm-up.  With ``sustain_s`` > 0 each also runs back
+    to back for that long while nvidia-smi samples clock and power, since at
+    large batches both settle at the board power limit."""
+    import torch
+    import lm_head_gumbel_gb300 as fs
+    d, V = w.d, w.V
+    entries = []
+    for B in batches:
+        _, inp = make_inputs_like(w, B, dev, W)
+        out = torch.empty(B, dtype=torch.int64, device=dev)
+        ws = torch.zeros(fs.fs_workspace_size(B, V), dtype=torch.uint8, device=dev)
+        logits = torch.empty(B, V, dtype=torch.bfloat16, device=dev)
+
+        def gemm(k):
+            torch.matmul(inp["H"], W.t(), out=logits)
+
+        def fused(k):
+            fs.fs_sample(inp["H"], W, temperature=inp["temperature"], seeds=inp["seeds"],
+                         vocab_mask=inp["vocab_mask"], offset=k, out_idx=out, workspace=ws,
+                         stream=stream)
+
+        ent = {"B": B}
+        with torch.cuda.stream(stream):
+            for name, fn in (("library_gemm", gemm), ("fused_sample", fused)):
+                for k in range(5):
+                    fn(k)
+                torch.cuda.synchronize()
+                us = time_calls(fn, steps, stream) * 1000.0 / steps
+                ent[f"{name}_us"] = round(us, 2)
+                ent[f"{name}_tflops"] = round(2.0 * B * V * d / us / 1e6, 1)
+            if sustain_s > 0:
+                sus = {}
+                for name, fn in (("library_gemm", gemm), ("fused_sample", fused)):
+                    sampler = ClockSampler(dev.index or 0)
+                    sampler.start()
+                    n, t0 = 0, time.time()
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    while time.time() - t0 < sustain_s:
+                        for k in range(50):
+                            fn(n + k)
+                        n += 50
+                        e1.record(stream)
+                        e1.synchronize()
+                    us = e0.elapsed_time(e1) * 1000.0 / n
+                    rows = sampler.stop()
+                    # the first half second is the ramp into the power limit
+                    rows = [r for r in rows if t0 + 0.5 <= r["t"] <= time.time()]
+                    watts = [float(r["power"]) for r in rows if r["power"].replace(".", "", 1).isdigit()]
+                    c = ClockSampler.summarize(rows, t0 + 0.5, time.time())
+                    p = statistics.median(watts) if watts else None
+                    sus[name] = {"us": round(us, 2), "calls": n,
+                                 "sm_mhz": None if c is None else c["sm_mhz"],
+                                 "power_w": p, "reasons": None if c is None else c["reasons"],
+                                 "joules_per_call": None if p is None else round(p * us * 1e-6, 4)}
+                    time.sleep(1.0)
+                ent["sustained"] = sus
+        entries.append(ent)
+        del inp, out, ws, logits
+    return {"what": "torch.matmul bf16 of the same H W^T (library GEMM, logits written, "
+                    "nothing sampled) vs the fused sampling call, same inputs",
+            "entries": entries}
 
 
 def oracle_inputs(inp):
