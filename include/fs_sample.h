@@ -115,7 +115,27 @@ typedef struct fs_sample_args {
    * tensor-parallel and Group-Gumbel-Max paragraphs; the largest logit for a
    * greedy row); needs out_tile_lse.  Adds a small second kernel. */
   float *out_lse;
+  /* FS_FLAG_* bits, 0 for none; unknown bits are FS_ERR_INVALID_ARG. */
+  uint32_t flags;
 } fs_sample_args;
+
+/*
+ * flags: overlap the kernel launched before this call on the same stream (a
+ * programmatic dependent launch).  The sampling kernel may then start while
+ * that kernel is still running, as its thread blocks leave SMs free, and
+ * stream the first slices of W into its shared-memory pipeline; it reads H,
+ * the temperatures, seeds and mask, and reads or writes the workspace and
+ * every output, only after the earlier kernel has completed and its writes
+ * are visible.  So the earlier kernel may produce H and the per-row inputs,
+ * but must not write W.  It hides the sampler's launch and pipeline fill
+ * behind the kernel that computes H (e.g. the final normalisation of a decode
+ * step).  When the earlier work on the stream is not a kernel, the call runs
+ * as without the flag.  The results are the same with or without it.  Used by
+ * fs_sample, fs_sample_noalloc, fs_sample_host (whose own copy kernel already
+ * overlaps it when in_bytes > 0) and fs_sample_topk.  The library's sampling
+ * kernels allow such a dependent to be scheduled as soon as they start.
+ */
+#define FS_FLAG_OVERLAP_PREVIOUS 1u
 
 /* Number of 128-wide vocabulary tiles, ceil(V / 128); 0 for V <= 0. */
 int64_t fs_num_tiles(int64_t V);

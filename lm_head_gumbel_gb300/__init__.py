@@ -5,7 +5,7 @@ package is its Python binding plus the seeded synthetic workloads used by the
 tests and the benchmark.
 """
 from ._binding import (FS_ERR_CUDA, FS_ERR_DEVICE_TIMEOUT, FS_ERR_INVALID_ARG,  # noqa: F401
-                       FS_ERR_UNSUPPORTED, FS_ERR_WORKSPACE, FS_MERGE_EXACT,
+                       FS_ERR_UNSUPPORTED, FS_ERR_WORKSPACE, FS_FLAG_OVERLAP_PREVIOUS, FS_MERGE_EXACT,
                        FS_MERGE_GROUP_GUMBEL, FS_OK, FS_SYNC_IDS, FS_SYNC_NONE, FS_SYNC_STREAM,
                        FS_TILE, FS_TOPK_MAX, LIB_PATH, FsError,
                        FsSampleArgs, fs_group_merge, fs_gumbel_noise, fs_gumbel_transform,

@@ -23,6 +23,7 @@ FS_ERR_DEVICE_TIMEOUT = 4
 FS_ERR_WORKSPACE = 5
 FS_TOPK_MAX = 16
 FS_SYNC_NONE, FS_SYNC_STREAM, FS_SYNC_IDS = 0, 1, 2
+FS_FLAG_OVERLAP_PREVIOUS = 1
 FS_MERGE_EXACT = 0
 FS_MERGE_GROUP_GUMBEL = 1
 
@@ -39,7 +40,7 @@ class FsError(RuntimeError):
 
 
 class FsSampleArgs(ctypes.Structure):
-    """Mirror of ``fs_sample_args`` (every field is 8 bytes wide)."""
+    """Mirror of ``fs_sample_args`` (8-byte fields, then the 32-bit flags)."""
     _fields_ = [
         ("H", _c_ptr), ("W", _c_ptr), ("temperature", _c_ptr),
         ("vocab_mask", _c_ptr), ("mask_ld", _c_i64), ("seeds", _c_ptr),
@@ -48,6 +49,7 @@ class FsSampleArgs(ctypes.Structure):
         ("out_idx", _c_ptr), ("out_tile_max", _c_ptr), ("out_tile_idx", _c_ptr),
         ("out_tile_lse", _c_ptr), ("workspace", _c_ptr), ("workspace_bytes", ctypes.c_size_t),
         ("vocab_offset", _c_i64), ("out_max", _c_ptr), ("out_lse", _c_ptr),
+        ("flags", ctypes.c_uint32),
     ]
 
 
@@ -149,7 +151,7 @@ def _check_2d(name, t, dtype):
 def fs_sample(H, W, *, temperature=None, vocab_mask=None, seeds=None, seed=0, offset=0,
               out_idx=None, out_tile_max=None, out_tile_idx=None, out_tile_lse=None,
               workspace=None, stream=None, reduce=True, vocab_offset=0, out_max=None,
-              out_lse=None):
+              out_lse=None, overlap_previous=False):
     """Sample one token id per row of H from softmax(H W^T / T) (masked).
 
     H: bf16 [B, d]; W: bf16 [V, d]; temperature: fp32 [B] or None (T = 1);
@@ -163,7 +165,9 @@ def fs_sample(H, W, *, temperature=None, vocab_mask=None, seeds=None, seed=0, of
     the per-tile outputs (required then) are written and None is returned.
     vocab_offset: global id of W's first row (W a vocabulary shard); out_max /
     out_lse: optional fp32 [B] row maximum / row log-mass (out_lse needs
-    out_tile_lse)."""
+    out_tile_lse).  overlap_previous: launch as a programmatic dependent of the
+    stream's previous kernel (FS_FLAG_OVERLAP_PREVIOUS: W starts streaming
+    while that kernel finishes; it may write H and the per-row inputs, not W)."""
     lib = load_library()
     _check_2d("H", H, torch.bfloat16)
     _check_2d("W", W, torch.bfloat16)
@@ -195,7 +199,8 @@ def fs_sample(H, W, *, temperature=None, vocab_mask=None, seeds=None, seed=0, of
         out_tile_lse=_ptr(out_tile_lse),
         workspace=_ptr(workspace) if reduce else None,
         workspace_bytes=(workspace.numel() * workspace.element_size()) if reduce else 0,
-        vocab_offset=int(vocab_offset), out_max=_ptr(out_max), out_lse=_ptr(out_lse))
+        vocab_offset=int(vocab_offset), out_max=_ptr(out_max), out_lse=_ptr(out_lse),
+        flags=FS_FLAG_OVERLAP_PREVIOUS if overlap_previous else 0)
     with torch.cuda.device(dev):
         st = lib.fs_sample(ctypes.byref(args), _stream_handle(stream, dev))
     if st != FS_OK:
@@ -243,10 +248,10 @@ def fs_topk_workspace_size(B: int, V: int, K: int) -> int:
 
 def fs_sample_topk(H, W, K, *, temperature=None, vocab_mask=None, seeds=None, seed=0, offset=0,
                    vocab_offset=0, out_topk_idx=None, out_topk_score=None, workspace=None,
-                   stream=None):
+                   stream=None, overlap_previous=False):
     """K draws without replacement per row (the K largest noisy scores, in
     draw order).  Returns out_topk_idx (int64 [B, K]); fills out_topk_score
-    (fp32 [B, K]) when given."""
+    (fp32 [B, K]) when given.  overlap_previous: as in fs_sample."""
     lib = load_library()
     _check_2d("H", H, torch.bfloat16)
     _check_2d("W", W, torch.bfloat16)
@@ -264,7 +269,7 @@ def fs_sample_topk(H, W, K, *, temperature=None, vocab_mask=None, seeds=None, se
         mask_ld=mask_ld, seeds=_ptr(seeds), seed=int(seed) & (2**64 - 1),
         offset=int(offset) & (2**64 - 1), B=B, d=d, V=V, ldh=H.stride(0), ldw=W.stride(0),
         workspace=_ptr(workspace), workspace_bytes=workspace.numel() * workspace.element_size(),
-        vocab_offset=int(vocab_offset))
+        vocab_offset=int(vocab_offset), flags=FS_FLAG_OVERLAP_PREVIOUS if overlap_previous else 0)
     with torch.cuda.device(dev):
         st = lib.fs_sample_topk(ctypes.byref(args), int(K), _ptr(out_topk_idx),
                                 _ptr(out_topk_score), _stream_handle(stream, dev))

@@ -542,6 +542,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
+  // A kernel launched after this one as a programmatic dependent may be
+  // scheduled from now on, on whatever SM resources are free (for another
+  // sampling call: the SMs this grid's blocks leave); it must wait for this
+  // grid to complete before it reads anything this grid writes.
+  ptx::grid_launch_dependents();
   const uint32_t tmem_base = *tmem_holder;
   const Waiter waiter{abort_flag, p.wait_limit_ns};
   const uint32_t h_bytes = p.h_box_rows * 128u;  // the H box; the W slice follows it
@@ -757,6 +762,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::cluster_sync();  // both CTAs' barriers exist before either uses the other's
   ptx::tc_fence_after();
+  ptx::grid_launch_dependents();  // as in stage1_kernel
   const uint32_t tmem_base = *tmem_holder;
   const Waiter waiter{abort_flag, p.wait_limit_ns};
 

@@ -224,6 +224,7 @@ fs_status check_inputs(const fs_sample_args* a) {
   if (a == nullptr) return FS_ERR_INVALID_ARG;
   const int64_t B = a->B, d = a->d, V = a->V;
   if (!a->H || !a->W) return FS_ERR_INVALID_ARG;
+  if ((a->flags & ~uint32_t(FS_FLAG_OVERLAP_PREVIOUS)) != 0) return FS_ERR_INVALID_ARG;
   if (B < 1 || B > 65535 || d < 1 || V < 1 || V > int64_t(0x7FFFFFFF)) return FS_ERR_INVALID_ARG;
   if (d > int64_t(0x7FFFFFFF) - kBlockK) return FS_ERR_INVALID_ARG;
   if (a->ldh < d || a->ldw < d || a->ldh % 8 != 0 || a->ldw % 8 != 0) return FS_ERR_INVALID_ARG;
@@ -393,7 +394,8 @@ bool w_in_buffer(const fs_sample_args* a, const void* buf, size_t bytes) {
 }  // namespace fs
 
 extern "C" fs_status fs_sample(const fs_sample_args* a, void* stream_ptr) {
-  return sample(a, nullptr, false, stream_ptr);
+  return sample(a, nullptr, a != nullptr && (a->flags & FS_FLAG_OVERLAP_PREVIOUS) != 0,
+                stream_ptr);
 }
 
 extern "C" size_t fs_topk_workspace_size(int64_t B, int64_t V, int64_t K) {
@@ -424,7 +426,8 @@ extern "C" fs_status fs_sample_topk(const fs_sample_args* a, int64_t K, int64_t*
   p.topk_idx = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(a->workspace) +
                                           size_t(B) * size_t(n_cand) * 4u);
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
-  const fs_status lst = run_stage1(a, cap == 4 ? kModeTop4 : kModeTop16, p, stream);
+  const fs_status lst = run_stage1(a, cap == 4 ? kModeTop4 : kModeTop16, p, stream,
+                                   (a->flags & FS_FLAG_OVERLAP_PREVIOUS) != 0);
   if (lst != FS_OK) return lst;
   return launch_topk_reduce(p.topk_score, p.topk_idx, B, fs_num_tiles(V), cap, K, out_topk_idx,
                             out_topk_score, stream);
@@ -520,7 +523,9 @@ extern "C" fs_status fs_sample_host(const fs_sample_args* a, const void* host_in
   // Inputs in: mapped host memory is read by SMs over the host link (on a
   // Grace host, NVLink-C2C: several times the copy engine's rate for a
   // decode-sized H); other host memory goes through cudaMemcpyAsync.
-  bool overlap = false;  // the sampling kernel overlaps the copy kernel
+  // The sampling kernel overlaps the copy kernel below, or, with no inputs to
+  // copy and the flag set, whatever kernel came before on the stream.
+  bool overlap = in_bytes == 0 && (a->flags & FS_FLAG_OVERLAP_PREVIOUS) != 0;
   if (in_bytes > 0) {
     const void* src = mapped_host(host_in);
     if (src != nullptr) {

@@ -4,7 +4,8 @@
  * step fs_sample_host, and argument errors.  Greedy rows (T = 0) must return
  * the argmax of the logits, which this program computes itself in double
  * precision from the same bf16 values (rows whose top-2 logits are closer than
- * 1e-3 are not judged).  Prints "ok" and exits 0 on success.
+ * 1e-3 are not judged); a call with FS_FLAG_OVERLAP_PREVIOUS must repeat the
+ * plain call's ids.  Prints "ok" and exits 0 on success.
  *
  * Built and run by tests/test_gpu_c_abi.py.
  */
@@ -123,6 +124,13 @@ int main(void) {
   int64_t first[5], again[5];
   CHECK(cudaMemcpy(first, dout, sizeof first, cudaMemcpyDeviceToHost) == cudaSuccess, "copy");
   for (int64_t b = 0; b < B; ++b) CHECK(first[b] >= 0 && first[b] < V, "id in range");
+
+  /* The same call launched to overlap the kernel before it: the same ids. */
+  a.flags = FS_FLAG_OVERLAP_PREVIOUS;
+  CHECK(fs_sample(&a, NULL) == FS_OK, "fs_sample T=1 overlapped");
+  CHECK(cudaMemcpy(again, dout, sizeof again, cudaMemcpyDeviceToHost) == cudaSuccess, "copy");
+  for (int64_t b = 0; b < B; ++b) CHECK(again[b] == first[b], "overlapped call = plain call");
+  a.flags = 0;
 
   /* The same call from host memory: H and T copied in, ids written back. */
   const size_t in_bytes = nh * 2 + 256;

@@ -93,6 +93,7 @@ def _args(**kw):
     (dict(vocab_offset=-4), 1), (dict(vocab_offset=6), 1), (dict(vocab_offset=2**31 - 4096), 1),
     (dict(out_max=0x90000, out_idx=None), 1), (dict(out_lse=0x90000), 1),
     (dict(B=65535, V=2**31 - 1, d=8, ldh=8, ldw=8), 1),  # work units beyond 32 bits
+    (dict(flags=2), 1), (dict(flags=0x80000001), 1),  # unknown flag bits
     (dict(), 5),                                   # sampling without a workspace
     (dict(out_tile_max=None, out_tile_idx=None), 5),
     (dict(out_tile_max=None, out_tile_idx=None, workspace=0x70000, workspace_bytes=511), 5),
@@ -186,3 +187,30 @@ def test_host_step_bad_arguments(lib):
     assert f(ctypes.byref(_args(**dict(ws, workspace=None))), hin, din, 64, hout, 1, None) == 5
     assert f(ctypes.byref(_args(**ws)), hin, din, 64, hout, 3, None) == 1          # bad sync
     assert f(ctypes.byref(_args(**ws)), hin, din, 64, hout, -1, None) == 1
+
+
+def test_struct_layout_matches_the_header(tmp_path):
+    """The ctypes mirror of fs_sample_args has the C compiler's size and
+    field offsets (a C program built against the header prints them)."""
+    import shutil
+    import subprocess
+    import lm_head_gumbel_gb300 as fs
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    names = [f[0] for f in fs.FsSampleArgs._fields_]
+    src = tmp_path / "layout.c"
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "fs_sample.h"',
+             "int main(void) {", '  printf("size %zu\\n", sizeof(fs_sample_args));']
+    lines += [f'  printf("{n} %zu\\n", offsetof(fs_sample_args, {n}));' for n in names]
+    lines += ['  printf("flag %u\\n", (unsigned)FS_FLAG_OVERLAP_PREVIOUS);', "  return 0;", "}"]
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-std=c99", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True)
+    out = dict(line.split() for line in subprocess.run([str(exe)], capture_output=True, text=True,
+                                                       check=True).stdout.splitlines())
+    assert int(out.pop("size")) == ctypes.sizeof(fs.FsSampleArgs)
+    assert int(out.pop("flag")) == fs.FS_FLAG_OVERLAP_PREVIOUS
+    for n in names:
+        assert int(out[n]) == getattr(fs.FsSampleArgs, n).offset, n
