@@ -3,7 +3,6 @@ flops, the roofline's bound and fractions, the DRAM-traffic record's gating on
 the kernel source, and the clock-sample summaries that decide whether a
 number is kept."""
 import json
-import os
 
 import pytest
 
