@@ -141,3 +141,50 @@ def test_overlapped_chain_in_a_cuda_graph():
         torch.cuda.synchronize()
         for k in range(4):
             assert torch.equal(outs[k].cpu(), want[k]), k
+
+
+def test_host_step_with_the_flag():
+    """fs_sample_host with inputs already on the device (in_bytes = 0) and the
+    flag: the sampling kernel overlaps the kernel before it (here the one that
+    wrote H), and the ids equal the plain device call's."""
+    import ctypes
+    B, V = 32, 20000
+    p = make_problem(B, 512, V, T=1.0, per_row_seeds=True, seed=36)
+    dev = p["H"].device
+    ws = torch.zeros(fs.fs_workspace_size(B, V), dtype=torch.uint8, device=dev)
+    want = fs.fs_sample(p["H"], p["W"], temperature=p["temperature"], seeds=p["seeds"], offset=2,
+                        workspace=ws).cpu()
+    H = torch.empty_like(p["H"])
+    out = torch.empty(B, dtype=torch.int64, device=dev)
+    host_out = torch.empty(B, dtype=torch.int64).pin_memory()
+    args = fs.FsSampleArgs(H=H.data_ptr(), W=p["W"].data_ptr(),
+                           temperature=p["temperature"].data_ptr(), seeds=p["seeds"].data_ptr(),
+                           offset=2, B=B, d=512, V=V, ldh=512, ldw=512, out_idx=out.data_ptr(),
+                           workspace=ws.data_ptr(), workspace_bytes=ws.numel(),
+                           flags=fs.FS_FLAG_OVERLAP_PREVIOUS)
+    for sync in (fs.FS_SYNC_STREAM, fs.FS_SYNC_IDS):
+        H.zero_()
+        torch.cuda.synchronize()
+        H.copy_(p["H"])  # the kernel just before the sampler writes H
+        fs.fs_sample_host(ctypes.byref(args), None, None, host_out, sync=sync)
+        assert torch.equal(host_out, want), sync
+
+
+def test_noalloc_entry_point_with_the_flag():
+    import ctypes
+    B, V = 16, 9000
+    p = make_problem(B, 256, V, T=0.8, seed=37)
+    dev = p["H"].device
+    want = fs.fs_sample(p["H"], p["W"], temperature=p["temperature"], seed=4, offset=1).cpu()
+    out = torch.empty(B, dtype=torch.int64, device=dev)
+    lib = fs.load_library()
+    a = fs.FsSampleArgs(H=p["H"].data_ptr(), W=p["W"].data_ptr(),
+                        temperature=p["temperature"].data_ptr(), seed=4, offset=1, B=B, d=256,
+                        V=V, ldh=256, ldw=256, out_idx=out.data_ptr(),
+                        flags=fs.FS_FLAG_OVERLAP_PREVIOUS)
+    s = torch.cuda.current_stream()
+    for _ in range(3):
+        out.fill_(-5)  # a kernel right before the call
+        assert lib.fs_sample_noalloc(ctypes.byref(a), ctypes.c_void_p(s.cuda_stream)) == fs.FS_OK
+        torch.cuda.synchronize()
+        assert torch.equal(out.cpu(), want)
