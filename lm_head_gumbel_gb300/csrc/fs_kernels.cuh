@@ -12,7 +12,7 @@
 // number of batch blocks, CTA pairs compute 256 x 256 units with cta_group::2
 // MMAs (stage1_pair_kernel below).  Single-CTA roles:
 //   warp 0    TMA producer: streams 64-wide K slices of W (256 x 64) and
-//             H (up to 128 x 64) into a shared-memory ring of 4-6 stages
+//             H (up to 128 x 64) into a shared-memory ring of 4-5 stages
 //             (128-byte swizzle; the fewer H rows, the more stages)
 //   warp 1    tcgen05 MMA issuer: M=128, N=256, K=16 bf16 MMAs accumulate the
 //             unit's logits in tensor memory (fp32, 256 columns); two
@@ -48,7 +48,7 @@ constexpr int kBlockM = 128;   // batch rows per unit = tensor-memory lanes
 constexpr int kBlockN = 256;   // vocabulary ids per unit = accumulator columns
 constexpr int kBlockK = 64;    // bf16 elements per 128-byte swizzled row
 constexpr int kUmmaK = 16;     // K of one kind::f16 MMA
-constexpr int kMaxStages = 6;  // ring depth: as many stages as fit kRingBytes, at most 6
+constexpr int kMaxStages = 5;  // ring depth: as many stages as fit kRingBytes, at most 5
 constexpr int kTileV = FS_TILE;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 32 * (2 + kEpiWarps);

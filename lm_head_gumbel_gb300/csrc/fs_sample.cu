@@ -258,7 +258,7 @@ fs_status run_stage1(const fs_sample_args* a, int mode, Stage1Params& p, cudaStr
   const int n_mt = int((B + kBlockM - 1) / kBlockM);
   // An even number of 128-row batch blocks: CTA pairs with M = 256 MMAs, each
   // CTA holding half of the W slice (six 32 KB stages).  Otherwise single
-  // CTAs with M = 128 and the whole slice (4-6 stages of H box + 32 KB); with
+  // CTAs with M = 128 and the whole slice (4-5 stages of H box + 32 KB); with
   // an odd number of batch blocks above one, pairs would leave half a pair idle.
   const bool pair = n_mt > 1 && n_mt % 2 == 0;
   CUtensorMap tmap_h, tmap_w;
