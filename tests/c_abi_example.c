@@ -5,7 +5,9 @@
  * the argmax of the logits, which this program computes itself in double
  * precision from the same bf16 values (rows whose top-2 logits are closer than
  * 1e-3 are not judged); a call with FS_FLAG_OVERLAP_PREVIOUS must repeat the
- * plain call's ids.  Prints "ok" and exits 0 on success.
+ * plain call's ids; three draws without replacement on greedy rows must be the
+ * three largest logits; two vocabulary shards merged exactly must give the
+ * unsharded sample.  Prints "ok" and exits 0 on success.
  *
  * Built and run by tests/test_gpu_c_abi.py.
  */
@@ -149,6 +151,87 @@ int main(void) {
         "fs_sample_host");
   for (int64_t b = 0; b < B; ++b) again[b] = host_out[b];
   for (int64_t b = 0; b < B; ++b) CHECK(again[b] == first[b], "host step = device call");
+
+  /* K draws without replacement, greedy rows: the K largest logits in order.
+   * Each row's three largest logits are found here in double precision; rows
+   * whose top logits are closer than 1e-3 are not judged. */
+  for (int64_t b = 0; b < B; ++b) hT[b] = 0.0f;
+  CHECK(cudaMemcpy(dT, hT, sizeof hT, cudaMemcpyHostToDevice) == cudaSuccess, "copy T");
+  {
+    const int64_t K = 3;
+    void* tk_ws = NULL;
+    int64_t* tk_out = NULL;
+    const size_t tk_bytes = fs_topk_workspace_size(B, V, K);
+    CHECK(tk_bytes > 0, "fs_topk_workspace_size");
+    CHECK(cudaMalloc(&tk_ws, tk_bytes) == cudaSuccess, "cudaMalloc top-K workspace");
+    CHECK(cudaMalloc((void**)&tk_out, B * K * sizeof(int64_t)) == cudaSuccess, "cudaMalloc top-K");
+    fs_sample_args t = a;
+    t.out_idx = NULL;
+    t.workspace = tk_ws;
+    t.workspace_bytes = tk_bytes;
+    CHECK(fs_sample_topk(&t, K, tk_out, NULL, NULL) == FS_OK, "fs_sample_topk");
+    int64_t got[5 * 3];
+    CHECK(cudaMemcpy(got, tk_out, sizeof got, cudaMemcpyDeviceToHost) == cudaSuccess, "copy");
+    int judged_k = 0;
+    for (int64_t b = 0; b < B; ++b) {
+      double top[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      int64_t arg[4] = {-1, -1, -1, -1};
+      for (int64_t v = 0; v < V; ++v) {
+        double l = 0.0;
+        for (int64_t k = 0; k < d; ++k) l += from_bf16(hH[b * d + k]) * from_bf16(hW[v * d + k]);
+        int q = 4;
+        while (q > 0 && l > top[q - 1]) --q;
+        if (q < 4) {
+          for (int r = 3; r > q; --r) {
+            top[r] = top[r - 1];
+            arg[r] = arg[r - 1];
+          }
+          top[q] = l;
+          arg[q] = v;
+        }
+      }
+      if (top[0] - top[1] > 1e-3 && top[1] - top[2] > 1e-3 && top[2] - top[3] > 1e-3) {
+        for (int q = 0; q < 3; ++q) CHECK(got[b * K + q] == arg[q], "top-K id is the q-th logit");
+        ++judged_k;
+      }
+    }
+    CHECK(judged_k >= 2, "enough clearly separated rows for top-K");
+    cudaFree(tk_ws);
+    cudaFree(tk_out);
+  }
+
+  /* Two vocabulary shards sampled with global ids, merged exactly: the same
+   * ids as the unsharded call (T = 1, the offset of `first`). */
+  for (int64_t b = 0; b < B; ++b) hT[b] = 1.0f;
+  CHECK(cudaMemcpy(dT, hT, sizeof hT, cudaMemcpyHostToDevice) == cudaSuccess, "copy T");
+  {
+    const int64_t cut = 1536; /* a multiple of 256: the shards keep the unsharded K order */
+    int64_t* z = NULL;
+    float* m = NULL;
+    int64_t* merged = NULL;
+    CHECK(cudaMalloc((void**)&z, 2 * B * sizeof(int64_t)) == cudaSuccess, "cudaMalloc z");
+    CHECK(cudaMalloc((void**)&m, 2 * B * sizeof(float)) == cudaSuccess, "cudaMalloc m");
+    CHECK(cudaMalloc((void**)&merged, B * sizeof(int64_t)) == cudaSuccess, "cudaMalloc merged");
+    for (int part = 0; part < 2; ++part) {
+      fs_sample_args s = a;
+      s.offset = 11;
+      s.W = (const char*)dW + (part ? cut * d * 2 : 0);
+      s.V = part ? V - cut : cut;
+      s.vocab_offset = part ? cut : 0;
+      s.out_idx = z + part * B;
+      s.out_max = m + part * B;
+      CHECK(fs_sample(&s, NULL) == FS_OK, "fs_sample on a shard");
+    }
+    CHECK(fs_group_merge(z, m, NULL, 2, B, FS_MERGE_EXACT, NULL, 7, 11, merged, NULL, NULL) ==
+              FS_OK,
+          "fs_group_merge");
+    int64_t mg[5];
+    CHECK(cudaMemcpy(mg, merged, sizeof mg, cudaMemcpyDeviceToHost) == cudaSuccess, "copy");
+    for (int64_t b = 0; b < B; ++b) CHECK(mg[b] == first[b], "merged shards = unsharded sample");
+    cudaFree(z);
+    cudaFree(m);
+    cudaFree(merged);
+  }
 
   /* Errors come back as status codes, before anything runs. */
   fs_sample_args bad = a;
