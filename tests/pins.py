@@ -288,6 +288,14 @@ def pin_lse_merge(o):
     for b in range(B):
         assert np.isclose(lse_merge(r["tile_lse"][b]),
                           scipy.special.logsumexp(L[b] / T), rtol=1e-12, atol=1e-12)
+    # large logits: the merge of tile log-masses near 1e3 must not overflow
+    Hb, Wb = make_problem(1, 16, 512, seed=4, scale=300.0)
+    rb = o.sample(Hb, Wb, temperature=np.full(1, 0.5, np.float32))
+    Lb = ref_logits(Hb, Wb)[0]
+    assert np.max(rb["tile_lse"][0]) > 800.0
+    got = lse_merge(rb["tile_lse"][0])
+    assert np.isfinite(got) and np.isclose(got, scipy.special.logsumexp(Lb / 0.5), rtol=1e-12)
+    assert lse_merge([-np.inf, -np.inf]) == -np.inf and lse_merge([]) == -np.inf
 
 
 # ---- distribution ------------------------------------------------------------
@@ -421,7 +429,130 @@ def pin_topk_plackett_luce(o):
     assert pval > P_MIN, pval
 
 
+# ---- the goodness-of-fit instrument and the merges themselves ---------------
+def pin_chi_square_instrument(o):
+    """The chi-square helper every distributional pin and GPU test relies on.
+
+    Without pooling it must reproduce scipy.stats.chisquare (statistic and
+    p-value); a pooled case worked by hand must give its closed form (two
+    degrees of freedom: p = exp(-x/2)); a count in a zero-probability
+    category must reject outright; and at the pins' own sample size it must
+    reject draws from a law a little off softmax(l / T) -- a flatter
+    temperature, or two probabilities swapped -- while accepting draws from
+    softmax(l / T) itself.  (The draws here come from numpy's multinomial, not
+    from the oracle.)"""
+    rng = np.random.default_rng(2024)
+    # unpooled: every expected count >= 5
+    for V, n in ((16, 20000), (64, 20000), (5, 300)):
+        p = rng.dirichlet(np.full(V, 4.0))
+        p = np.maximum(p, 0.01)
+        p /= p.sum()
+        counts = rng.multinomial(n, p)
+        stat, dof, pval = chi_square_gof(counts, p)
+        ref = scipy.stats.chisquare(counts, p * n)
+        assert dof == V - 1, (V, dof)
+        assert math.isclose(stat, ref.statistic, rel_tol=1e-12, abs_tol=1e-12), (stat, ref)
+        assert math.isclose(pval, ref.pvalue, rel_tol=1e-10, abs_tol=1e-300), (pval, ref)
+    # pooled, by hand: n = 100, expected (60, 30, 4, 3, 3) -> bins (60, 30, 10);
+    # observed (55, 32, 5, 4, 4) -> (55, 32, 13);
+    # x = 25/60 + 4/30 + 9/10 = 1.45 on 2 degrees of freedom, p = exp(-0.725)
+    stat, dof, pval = chi_square_gof([55, 32, 5, 4, 4], [0.6, 0.3, 0.04, 0.03, 0.03])
+    assert dof == 2 and math.isclose(stat, 1.45, rel_tol=1e-12), (stat, dof)
+    assert math.isclose(pval, math.exp(-0.725), rel_tol=1e-12), pval
+    # an impossible outcome observed
+    stat, dof, pval = chi_square_gof([10, 10, 1], [0.5, 0.5, 0.0])
+    assert pval == 0.0, (stat, dof, pval)
+    # the pins' own laws: accept the law, reject a nearby one
+    for (V, d, T, seed) in ((16, 16, 0.7, 11), (64, 8, 1.0, 12)):
+        H, W = make_problem(1, d, V, seed=seed)
+        lg = ref_logits(H, W)[0]
+        p = scipy.special.softmax(lg / T)
+        n = 20000
+        _, _, p_ok = chi_square_gof(rng.multinomial(n, p), p)
+        assert p_ok > P_MIN, (V, p_ok)
+        flat = scipy.special.softmax(lg / (1.15 * T))
+        _, _, p_flat = chi_square_gof(rng.multinomial(n, flat), p)
+        assert p_flat < P_MIN, (V, "flatter law accepted", p_flat)
+        order = np.argsort(p)
+        swapped = p.copy()
+        hi, mid = order[-1], order[V // 2]
+        swapped[hi], swapped[mid] = p[mid], p[hi]
+        _, _, p_swap = chi_square_gof(rng.multinomial(n, swapped), p)
+        assert p_swap < P_MIN, (V, "swapped law accepted", p_swap)
+
+
+def pin_group_gumbel_max_law(o):
+    """Group-Gumbel-Max picks group k with probability exp(L_k) / sum exp(L)
+    (hierarchical factorisation of the categorical): four groups of unequal
+    mass, fresh uniforms from numpy, counts against that law with scipy's
+    chi-square; a shift of every L_k changes nothing; a group of zero mass is
+    never picked, and with no group left the draw is -1."""
+    rng = np.random.default_rng(5)
+    p = np.array([0.55, 0.25, 0.12, 0.08])
+    z = np.array([101, 202, 303, 404])
+    n = 20000
+    for shift in (0.0, 700.0, -300.0):
+        L = np.log(p) + shift
+        picks = np.array([group_gumbel_max(z, L, rng.random(4)) for _ in range(n)])
+        counts = np.array([np.sum(picks == zk) for zk in z])
+        assert counts.sum() == n
+        pval = scipy.stats.chisquare(counts, p * n).pvalue
+        assert pval > P_MIN, (shift, counts, pval)
+    L = np.array([np.log(0.5), -np.inf, np.log(0.5), -np.inf])
+    picks = {group_gumbel_max(z, L, rng.random(4)) for _ in range(500)}
+    assert picks == {101, 303}, picks
+    assert group_gumbel_max(z, np.full(4, -np.inf), rng.random(4)) == -1
+
+
+def pin_online_merge_law(o):
+    """The online binary merge ends in group k with probability
+    exp(L_k) / sum exp(L) whatever the order the groups arrive in, and its
+    running log-mass ends at scipy's logsumexp of the L_k; groups of zero
+    mass leave the state alone."""
+    rng = np.random.default_rng(6)
+    p = np.array([0.1, 0.45, 0.05, 0.25, 0.15])
+    z = np.arange(10, 15)
+    L = np.log(p) + 3.0
+    n = 20000
+    finals = np.empty(n, dtype=np.int64)
+    for i in range(n):
+        zi, Li = online_merge(z, L, rng.random(len(z)))
+        finals[i] = zi
+    assert math.isclose(Li, scipy.special.logsumexp(L), rel_tol=1e-12, abs_tol=1e-12), Li
+    counts = np.bincount(finals - 10, minlength=len(z))
+    pval = scipy.stats.chisquare(counts, p * n).pvalue
+    assert pval > P_MIN, (counts, pval)
+    zl, Ll = online_merge([7, 8, 9], [0.0, -np.inf, -np.inf], rng.random(3))
+    assert zl == 7 and Ll == 0.0
+
+
+def pin_partition_ties(o):
+    """Exact ties between tiles and between partitions (greedy rows with
+    duplicated W rows) resolve to the lowest id, as numpy.argmax's first
+    occurrence does: the partition merge keeps the earlier tile and the
+    earlier partition."""
+    B, d, V = 3, 16, 1024
+    H, W = make_problem(B, d, V, seed=17)
+    L0 = ref_logits(H, W)
+    for b in range(B):
+        best = int(np.argmax(L0[b]))
+        # copies of the row's best W row in later tiles and later partitions
+        for v in (best + 1, 300, 640, 1023):
+            if v > best:
+                W[v] = W[best]
+    L = ref_logits(H, W)
+    r = o.sample(H, W, temperature=np.zeros(B, np.float32))
+    nt = r["tile_max"].shape[1]
+    for b in range(B):
+        want = int(np.argmax(L[b]))
+        assert r["idx"][b] == want
+        for bounds in ([0, nt], [0, 1, nt], [0, 2, 3, 5, nt], list(range(nt + 1))):
+            i, m = partition_argmax(r["tile_max"][b], r["tile_idx"][b], bounds)
+            assert i == want, (b, bounds, i, want)
+
+
 ALL_PINS = [
+    pin_chi_square_instrument,
     pin_philox_kat,
     pin_uniform_map,
     pin_gumbel_closed_forms,
@@ -430,7 +561,10 @@ ALL_PINS = [
     pin_tile_outputs,
     pin_fully_masked_row,
     pin_partition_invariance,
+    pin_partition_ties,
     pin_lse_merge,
+    pin_group_gumbel_max_law,
+    pin_online_merge_law,
     pin_noise_distribution,
     pin_noise_independence,
     pin_two_way_closed_form,

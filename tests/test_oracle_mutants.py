@@ -3,19 +3,27 @@ check that at least one pin (tests/pins.py) fails on it.
 
 This is how the pins are shown to be strong enough: a dropped term, a wrong
 sign, index, constant or operand anywhere in the oracle must be caught.  The
-mistakes are planted in a temporary copy of ``oracle/fs_oracle.c`` on the CPU;
-the committed oracle is never modified.
+mistakes are planted in a temporary copy of ``oracle/fs_oracle.c`` (compiled
+to its own library) or of ``oracle/merge.py`` (loaded as a separate module and
+handed to the pins in place of the real merges), on the CPU; the committed
+oracle is never modified.
 """
 import os
 import tempfile
+import types
 
 import pytest
 
 import oracle
+import oracle.merge
+import pins
 from oracle import build as obuild
 from pins import ALL_PINS
 
 SRC = open(obuild.SOURCE).read()
+MERGE_SRC = open(oracle.merge.__file__).read()
+MERGE_NAMES = ("chi_square_gof", "group_gumbel_max", "lse_merge", "online_merge",
+               "partition_argmax")
 
 # (name, text in fs_oracle.c, replacement, which occurrence (0 = first))
 MUTANTS = [
@@ -59,12 +67,49 @@ MUTANTS = [
 ]
 
 
-def mutate(name, old, new, which):
+# The same for oracle/merge.py: the group merges and the goodness-of-fit
+# instrument behind every distributional pin.
+MERGE_MUTANTS = [
+    ("ggm-noise-sign", "keys = L - np.log(-np.log(u))", "keys = L + np.log(-np.log(u))", 0),
+    ("ggm-single-log", "keys = L - np.log(-np.log(u))", "keys = L - np.log(u)", 0),
+    ("ggm-ignores-mass", "keys = L - np.log(-np.log(u))", "keys = -np.log(-np.log(u))", 0),
+    ("online-switch-reversed", "if u[k] < np.exp(Lk - new_L):", "if u[k] > np.exp(Lk - new_L):", 0),
+    ("online-max-not-logaddexp", "new_L = np.logaddexp(cur_L, Lk)", "new_L = max(cur_L, Lk)", 0),
+    ("online-old-mass", "if u[k] < np.exp(Lk - new_L):", "if u[k] < np.exp(Lk - cur_L):", 0),
+    ("partition-tie-in-partition", "tile_max[t] > m_p", "tile_max[t] >= m_p", 0),
+    ("partition-tie-across", "m_p > best_m", "m_p >= best_m", 0),
+    ("lse-merge-no-shift", "return float(m + np.log(np.sum(np.exp(a - m))))",
+     "return float(np.log(np.sum(np.exp(a))))", 0),
+    ("chi-square-over-n", "stat = float(np.sum((obs_b[keep] - exp_b[keep]) ** 2 / exp_b[keep]))",
+     "stat = float(np.sum((obs_b[keep] - exp_b[keep]) ** 2 / exp_b[keep])) / n", 0),
+    ("chi-square-observed-denominator", "** 2 / exp_b[keep]))", "** 2 / np.maximum(obs_b[keep], 1.0)))", 0),
+    ("chi-square-dof-not-minus-one", "dof = int(keep.sum() - 1)", "dof = int(keep.sum())", 0),
+    ("chi-square-pool-dropped", "obs_b.append(counts[~big].sum())\n        exp_b.append(exp[~big].sum())",
+     "pass", 0),
+    ("chi-square-impossible-ignored", "if np.any(obs_b[~keep] > 0):", "if False:", 0),
+    ("chi-square-sf-of-half", "float(chi2.sf(stat, dof))", "float(chi2.sf(stat / 2, dof))", 0),
+]
+
+
+def replace_nth(text, name, old, new, which, what):
     start = -1
     for _ in range(which + 1):
-        start = SRC.find(old, start + 1)
-        assert start >= 0, f"mutant {name}: text not found in fs_oracle.c"
-    return SRC[:start] + new + SRC[start + len(old):]
+        start = text.find(old, start + 1)
+        assert start >= 0, f"mutant {name}: text not found in {what}"
+    return text[:start] + new + text[start + len(old):]
+
+
+def mutate(name, old, new, which):
+    return replace_nth(SRC, name, old, new, which, "fs_oracle.c")
+
+
+def first_failing_pin(o):
+    for pin in ALL_PINS:
+        try:
+            pin(o)
+        except (AssertionError, ValueError, FloatingPointError, ZeroDivisionError, IndexError):
+            return pin.__name__
+    return None
 
 
 @pytest.fixture(scope="module")
@@ -78,14 +123,24 @@ def test_mutant_is_caught(workdir, name, old, new, which):
     text = mutate(name, old, new, which)
     lib = obuild.build_variant(text, name.replace("-", "_"), workdir)
     o = oracle.Oracle(lib)
-    caught = []
-    for pin in ALL_PINS:
-        try:
-            pin(o)
-        except AssertionError:
-            caught.append(pin.__name__)
-            break
-        except (ValueError, FloatingPointError, ZeroDivisionError, IndexError):
-            caught.append(pin.__name__)
-            break
-    assert caught, f"no pin catches the planted mistake {name!r}"
+    assert first_failing_pin(o), f"no pin catches the planted mistake {name!r}"
+
+
+@pytest.mark.parametrize("name,old,new,which", MERGE_MUTANTS, ids=[m[0] for m in MERGE_MUTANTS])
+def test_merge_mutant_is_caught(monkeypatch, name, old, new, which):
+    text = replace_nth(MERGE_SRC, name, old, new, which, "merge.py")
+    mod = types.ModuleType(f"merge_mutant_{name.replace('-', '_')}")
+    exec(compile(text, f"<merge.py: {name}>", "exec"), mod.__dict__)
+    for fn in MERGE_NAMES:
+        monkeypatch.setattr(pins, fn, getattr(mod, fn))
+    assert first_failing_pin(oracle.default()), f"no pin catches the planted mistake {name!r}"
+
+
+def test_merge_mutants_reach_the_pins(monkeypatch):
+    """Control for the test above: the real merge module, loaded the same way,
+    passes every pin (so a caught mutant is caught for its mistake)."""
+    mod = types.ModuleType("merge_unmodified")
+    exec(compile(MERGE_SRC, "<merge.py>", "exec"), mod.__dict__)
+    for fn in MERGE_NAMES:
+        monkeypatch.setattr(pins, fn, getattr(mod, fn))
+    assert first_failing_pin(oracle.default()) is None
