@@ -255,6 +255,7 @@ def time_calls(fn, steps, stream):
 def run_ours(args):
     import torch
     import lm_head_gumbel_gb300 as fs
+    from lm_head_gumbel_gb300 import workloads as wl_mod
 
     world, rank, local = dist_init("nccl")
     torch.cuda.set_device(local)
@@ -291,31 +292,8 @@ def run_ours(args):
     sweep = []
     if not args.no_sweep and world == 1:
         for b2 in w.batches:
-            _, inp2 = make_inputs_like(w, b2, dev, inp["W"])
-            o2 = torch.empty(b2, dtype=torch.int64, device=dev)
-            ws2 = torch.zeros(fs.fs_workspace_size(b2, V), dtype=torch.uint8, device=dev)
-            t2 = tile_outputs(w, b2, dev)
-
-            def c2(k):
-                fs.fs_sample(inp2["H"], inp2["W"], temperature=inp2["temperature"],
-                             seeds=inp2["seeds"], vocab_mask=inp2["vocab_mask"], offset=k,
-                             out_idx=o2, workspace=ws2, stream=stream, **t2)
-
-            for k in range(5):
-                c2(k)
-            torch.cuda.synchronize()
-            ts0 = time.time()
-            us2 = time_calls(c2, args.sweep_steps, stream) * 1000.0 / args.sweep_steps
-            rf = roofline(b2, d, V, us2, peaks, seeds=inp2["seeds"] is not None,
-                          mask=inp2["vocab_mask"] is not None, tiles=bool(t2))
-            ent = {"B": b2, "us_per_call": round(us2, 2),
-                   "tokens_per_s": round(b2 / (us2 * 1e-6), 1), "bound": rf["bound"],
-                   "achieved": rf["achieved"], "unit": rf["unit"], "frac": rf["frac"],
-                   "window": (ts0, time.time())}
-            if "frac_of_sustained" in rf:
-                ent["frac_of_sustained"] = rf["frac_of_sustained"]
-            sweep.append(ent)
-            del inp2, o2, ws2, t2
+            sweep.append(time_point(w, args.workload, b2, inp["W"], dev, stream, peaks,
+                                    args.sweep_steps))
     # The K-draws-without-replacement mode on the same batch (an extension of
     # the headline path; reported beside it, not in it).
     extensions = {}
@@ -407,10 +385,29 @@ def run_ours(args):
     h2d = host_in.numel()  # bytes copied host -> device per step (inputs + alignment pad)
     d2h = out_h.numel() * 8
 
+    # Every other workload of the benchmark set, each with its own head, batch
+    # sizes, temperature law, mask and tile outputs (same run, same clocks).
+    others = {}
+    if not args.no_sweep and world == 1:
+        for name in OTHER_WORKLOADS:
+            if name == args.workload:
+                continue
+            wo = wl_mod.WORKLOADS[name]
+            Wo = wl_mod.make_weights(wo.d, wo.V, seed=77, device=dev,
+                                     outlier_frac=wo.outlier_frac)
+            pts = [time_point(wo, name, bo, Wo, dev, stream, peaks, args.sweep_steps)
+                   for bo in wo.batches]
+            others[name] = {"config": describe(wo, "/".join(str(x) for x in wo.batches)),
+                            "l2": l2_note(wo.V, wo.d), "points": pts}
+            del Wo
+            torch.cuda.empty_cache()
+
     clock_rows = clocks.stop()
-    for ent in sweep:  # clocks seen while each batch size ran
+    # clocks seen while each batch size ran
+    for ent in sweep + [p for o in others.values() for p in o["points"]]:
         c = ClockSampler.summarize(clock_rows, *ent.pop("window"))
         ent["sm_mhz"] = None if c is None else c["sm_mhz"]
+        ent["clock_reasons"] = None if c is None else c["reasons"]
     st, code = fs.fs_last_device_error()
     if st != fs.FS_OK:
         raise SystemExit(f"device error word {code} after the benchmark")
@@ -437,9 +434,7 @@ def run_ours(args):
         "config": {
             "workload": describe(w, B),
             "B": B, "d": d, "V": V, "global_batch": B * world,
-            "l2": (("inputs exceed L2 (W is %.2f GB), no flush" % (V * d * 2 / 1e9))
-                   if V * d * 2 > L2_BYTES else
-                   ("W (%.1f MB) fits in L2: warm, no flush" % (V * d * 2 / 1e6))),
+            "l2": l2_note(V, d),
             "parallelism": "replicas" if world > 1 else "single-gpu",
         },
         "tokens_per_s": round(B * world / (us_call * 1e-6), 1),
@@ -449,6 +444,7 @@ def run_ours(args):
         "gpu_launches": args.steps,
         "clocks": ClockSampler.summarize(clock_rows, t_wall0, t_wall1),
         "sweep": sweep,
+        "workloads": others,
         "extensions": extensions,
     }
     if world == 1 and args.library_gemm:
@@ -462,6 +458,48 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+# The benchmark set beside the headline head: each is timed in the default run.
+OTHER_WORKLOADS = ("qwen3-8b", "qwen3-1.7b", "llama3-8b-mask", "large-vocab", "tiny")
+
+
+def l2_note(V, d):
+    return (("inputs exceed L2 (W is %.2f GB), no flush" % (V * d * 2 / 1e9))
+            if V * d * 2 > L2_BYTES else
+            ("W (%.1f MB) fits in L2: warm, no flush" % (V * d * 2 / 1e6)))
+
+
+def time_point(w, name, B, W, dev, stream, peaks, steps):
+    """One (workload, batch) point: `steps` sampling calls back to back, with
+    the workload's own per-row inputs and tile outputs, offset = step."""
+    import torch
+    import lm_head_gumbel_gb300 as fs
+    d, V = w.d, w.V
+    _, inp = make_inputs_like(w, B, dev, W)
+    out = torch.empty(B, dtype=torch.int64, device=dev)
+    ws = torch.zeros(fs.fs_workspace_size(B, V), dtype=torch.uint8, device=dev)
+    t = tile_outputs(w, B, dev)
+
+    def call(k):
+        fs.fs_sample(inp["H"], W, temperature=inp["temperature"], seeds=inp["seeds"],
+                     vocab_mask=inp["vocab_mask"], offset=k, out_idx=out, workspace=ws,
+                     stream=stream, **t)
+
+    for k in range(5):
+        call(k)
+    torch.cuda.synchronize()
+    ts0 = time.time()
+    us = time_calls(call, steps, stream) * 1000.0 / steps
+    rf = roofline(B, d, V, us, peaks, traffic=measured_traffic(name, B),
+                  seeds=inp["seeds"] is not None, mask=inp["vocab_mask"] is not None,
+                  tiles=bool(t))
+    ent = {"B": B, "us_per_call": round(us, 2), "tokens_per_s": round(B / (us * 1e-6), 1),
+           "bound": rf["bound"], "achieved": rf["achieved"], "unit": rf["unit"],
+           "frac": rf["frac"], "traffic": rf["traffic"], "window": (ts0, time.time())}
+    if "frac_of_sustained" in rf:
+        ent["frac_of_sustained"] = rf["frac_of_sustained"]
+    return ent
 
 
 def make_inputs_like(w, B, device, W):

@@ -180,9 +180,10 @@ fs_status fs_sample(const fs_sample_args *args, void *stream);
  *   FS_ERR_WORKSPACE before anything is launched.  Calls that only write
  *   per-tile outputs use no scratch.
  * - Set-up: the first call on a device (with that device current) looks up the
- *   array's device address and clears the array once (a synchronous
- *   cudaMemset, not an allocation); make that first call before any stream
- *   capture.
+ *   array's device address and clears the array once, with a memset (not an
+ *   allocation) enqueued on that call's stream ahead of its kernel, so the
+ *   first call may come on any stream, blocking or not; make that first call
+ *   before any stream capture.
  * - Sharing: every call on a device uses the same array.  The array must be
  *   all-zero when a call starts, and every call leaves it all-zero.  Calls that
  *   overlap on the GPU (concurrent streams) race on it; serialise them.
@@ -319,13 +320,24 @@ fs_status fs_gumbel_transform(const uint32_t *words, int64_t n, float *out, void
 fs_status fs_wait_timeout_selftest(uint64_t limit_ns, void *stream);
 
 /*
- * Read and clear the device-side error word of the current device (this
- * synchronises the device).  *code receives the raw word (0 = none; bit 0: a
- * bounded pipeline wait timed out).  Returns FS_ERR_DEVICE_TIMEOUT if a wait
- * timed out since the last read, FS_OK otherwise, FS_ERR_CUDA on a failed
- * read.
+ * Read and clear the device-side error word of the current device, after the
+ * work enqueued on `stream` so far (a cudaStream_t; NULL = the legacy default
+ * stream): the read is a one-thread kernel and a copy on that stream, and the
+ * call waits for that stream only.  *code receives the raw word (0 = none;
+ * bit 0: a bounded pipeline wait timed out).  Returns FS_ERR_DEVICE_TIMEOUT if
+ * a wait timed out since the last read, FS_OK otherwise, FS_ERR_CUDA on a
+ * failed launch, copy or wait.
+ * Scope: the word is one per device, not per stream or per call: every
+ * sampling kernel on the device records its timeouts in it, so a timeout in a
+ * call on another stream (or by another caller) is reported to whichever call
+ * of this function reads it first, and one that is still running when this
+ * call reads is reported by a later read.  A timeout means a pipeline wait
+ * went 2 s without progress -- the device is in trouble for every caller --
+ * so one report per device is what the word is for.  Two calls of this
+ * function on one device at the same time share one snapshot word; serialise
+ * them.
  */
-fs_status fs_last_device_error(int *code);
+fs_status fs_last_device_error(void *stream, int *code);
 
 /* Human-readable name of a status code (static storage). */
 const char *fs_status_string(int status);

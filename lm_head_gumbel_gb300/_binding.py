@@ -93,7 +93,7 @@ def load_library(path: str = LIB_PATH):
     lib.fs_online_merge.restype = ctypes.c_int
     lib.fs_wait_timeout_selftest.argtypes = [_c_u64, _c_ptr]
     lib.fs_wait_timeout_selftest.restype = ctypes.c_int
-    lib.fs_last_device_error.argtypes = [ctypes.POINTER(ctypes.c_int)]
+    lib.fs_last_device_error.argtypes = [_c_ptr, ctypes.POINTER(ctypes.c_int)]
     lib.fs_last_device_error.restype = ctypes.c_int
     lib.fs_status_string.argtypes = [ctypes.c_int]
     lib.fs_status_string.restype = ctypes.c_char_p
@@ -125,10 +125,15 @@ def fs_status_string(status: int) -> str:
     return load_library().fs_status_string(int(status)).decode()
 
 
-def fs_last_device_error():
-    """(status, raw error word) of the current device; synchronises it."""
+def fs_last_device_error(stream=None, device=None):
+    """(status, raw error word) of the device, read and cleared after the work
+    enqueued on `stream` (default: the current stream), waiting for that
+    stream only.  The word is one per device (see the header)."""
     code = ctypes.c_int(0)
-    st = load_library().fs_last_device_error(ctypes.byref(code))
+    device = torch.device(device or "cuda")
+    with torch.cuda.device(device):
+        st = load_library().fs_last_device_error(_stream_handle(stream, device),
+                                                 ctypes.byref(code))
     return int(st), int(code.value)
 
 

@@ -456,9 +456,13 @@ namespace fs {
 namespace {
 void* g_noalloc_addr[kMaxDevices] = {};
 
-// Device address of g_noalloc_scratch on the current device (looked up, and
-// the array cleared, on the first call per device).
-fs_status noalloc_scratch(void** out) {
+// Device address of g_noalloc_scratch on the current device, looked up on the
+// first call per device.  That call also clears the array with a memset
+// enqueued on the caller's stream, so the sampling kernel that follows on the
+// same stream sees it cleared whatever kind of stream it is (a plain
+// cudaMemset would go to the legacy default stream, which a non-blocking
+// stream does not wait for).
+fs_status noalloc_scratch(cudaStream_t stream, void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     cudaGetLastError();
@@ -468,7 +472,7 @@ fs_status noalloc_scratch(void** out) {
   if (g_noalloc_addr[dev] == nullptr) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr ||
-        cudaMemset(p, 0, FS_NOALLOC_SCRATCH_BYTES) != cudaSuccess) {
+        cudaMemsetAsync(p, 0, FS_NOALLOC_SCRATCH_BYTES, stream) != cudaSuccess) {
       cudaGetLastError();
       return FS_ERR_CUDA;
     }
@@ -491,7 +495,7 @@ extern "C" fs_status fs_sample_noalloc(const fs_sample_args* a, void* stream_ptr
   const fs_status st = device_setup(&num_sms);
   if (st != FS_OK) return st;
   void* scratch = nullptr;
-  const fs_status st2 = noalloc_scratch(&scratch);
+  const fs_status st2 = noalloc_scratch(static_cast<cudaStream_t>(stream_ptr), &scratch);
   if (st2 != FS_OK) return st2;
   fs_sample_args b = *a;
   b.workspace = scratch;
@@ -614,15 +618,21 @@ extern "C" fs_status fs_wait_timeout_selftest(uint64_t limit_ns, void* stream_pt
   return cudaGetLastError() == cudaSuccess ? FS_OK : FS_ERR_CUDA;
 }
 
-extern "C" fs_status fs_last_device_error(int* code) {
+namespace fs {
+// Take the device error word (read it and clear it in one atomic step) into
+// g_error_taken, ordered on the stream of the caller that asks for it.
+__device__ int g_error_taken = 0;
+__global__ void take_error_word_kernel() { g_error_taken = atomicExch(&g_error_word, 0); }
+}  // namespace fs
+
+extern "C" fs_status fs_last_device_error(void* stream_ptr, int* code) {
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   int v = 0;
-  if (cudaDeviceSynchronize() != cudaSuccess ||
-      cudaMemcpyFromSymbol(&v, g_error_word, sizeof(int)) != cudaSuccess) {
-    cudaGetLastError();
-    return FS_ERR_CUDA;
-  }
-  const int zero = 0;
-  if (v != 0 && cudaMemcpyToSymbol(g_error_word, &zero, sizeof(int)) != cudaSuccess) {
+  take_error_word_kernel<<<1, 1, 0, stream>>>();
+  if (cudaGetLastError() != cudaSuccess ||
+      cudaMemcpyFromSymbolAsync(&v, g_error_taken, sizeof(int), 0, cudaMemcpyDeviceToHost,
+                                stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess) {
     cudaGetLastError();
     return FS_ERR_CUDA;
   }

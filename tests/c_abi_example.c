@@ -242,7 +242,7 @@ int main(void) {
   CHECK(fs_sample(&bad, NULL) == FS_ERR_WORKSPACE, "missing workspace rejected");
   CHECK(strcmp(fs_status_string(FS_ERR_WORKSPACE), "FS_ERR_WORKSPACE") == 0, "status string");
   int code = -1;
-  CHECK(fs_last_device_error(&code) == FS_OK && code == 0, "no device error");
+  CHECK(fs_last_device_error(NULL, &code) == FS_OK && code == 0, "no device error");
 
   cudaFreeHost(host_in);
   cudaFreeHost(host_out);

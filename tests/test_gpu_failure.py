@@ -36,6 +36,19 @@ def test_context_usable_after_timeout():
     assert fs.fs_last_device_error() == (fs.FS_OK, 0)
 
 
+def test_timeout_read_on_another_stream():
+    """The word is one per device: a timeout raised by a kernel on one stream
+    is reported by a read ordered on another stream once that kernel is done,
+    and the read waits for its own stream only."""
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        fs.fs_wait_timeout_selftest(1_000_000)
+    side.synchronize()
+    st, code = fs.fs_last_device_error(stream=torch.cuda.current_stream())
+    assert st == fs.FS_ERR_DEVICE_TIMEOUT and code & 1
+    assert fs.fs_last_device_error(stream=side) == (fs.FS_OK, 0)
+
+
 def test_selftest_rejects_limits_out_of_range():
     for bad in (0, 999, 2_000_000_000):
         with pytest.raises(fs.FsError):

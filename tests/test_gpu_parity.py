@@ -155,10 +155,11 @@ def test_deterministic_across_calls_and_streams():
 @pytest.mark.parametrize("V", [40000, 151936])
 def test_rows_do_not_depend_on_the_batch(V):
     """A row's tile outputs and sample are bit-identical whatever batch it sits
-    in: B = 64 (one batch block: balanced runs of tiles, 128-id units where a
-    run cuts a vocabulary block), B = 384 (three batch blocks: single CTAs,
-    256-id units) and B = 256 (CTA pairs).  Every tile keeps its vocabulary
-    block's K order, so only the MMA shape differs."""
+    in: B = 64 (one batch block: single CTAs, M = 128 MMAs with an H box of
+    64 rows), B = 384 (three batch blocks: single CTAs, M = 128) and B = 256
+    (CTA pairs, M = 256).  Every unit covers 256 vocabulary ids and starts its
+    K loop at its vocabulary block's own slice, so only the MMA shape
+    differs."""
     big = make_problem(384, 512, V, T="row-uniform", per_row_seeds=True, seed=12)
     runs = {}
     for B in (64, 256, 384):
