@@ -11,13 +11,14 @@
 // vocabulary block of the logits l = H W^T, computed by one CTA; for an even
 // number of batch blocks, CTA pairs compute 256 x 256 units with cta_group::2
 // MMAs (stage1_pair_kernel below).  Single-CTA roles:
-//   warp 0    TMA producer: streams 64-wide K slices of W (256 x 64) and
-//             H (up to 128 x 64) into a shared-memory ring of 4-5 stages
-//             (128-byte swizzle; the fewer H rows, the more stages)
-//   warp 1    tcgen05 MMA issuer: M=128, N=256, K=16 bf16 MMAs accumulate the
-//             unit's logits in tensor memory (fp32, 256 columns); two
-//             accumulators so the epilogue of one unit overlaps the MMAs of
-//             the next
+//   warp 0    TMA producer (one elected lane issues): streams 64-wide K
+//             slices of W (256 x 64) and H (up to 128 x 64) into a shared-
+//             memory ring of 4-5 stages (128-byte swizzle; the fewer H rows,
+//             the more stages)
+//   warp 1    tcgen05 MMA issuer (one elected lane issues): M=128, N=256,
+//             K=16 bf16 MMAs accumulate the unit's logits in tensor memory
+//             (fp32, 256 columns); two accumulators so the epilogue of one
+//             unit overlaps the MMAs of the next
 //   warps 2-9 epilogue: each thread owns one batch row and 128 vocabulary
 //             columns (one output tile); it reads its logits from tensor
 //             memory, scales by 1/T, masks, adds Philox Gumbel noise, and
@@ -127,6 +128,11 @@ struct Waiter {
         return false;
       }
     }
+  }
+  // The same wait for a warp whose lanes all poll the barrier: every lane
+  // gets the same answer (a lane that gave up makes the whole warp give up).
+  __device__ bool wait_warp(uint64_t* bar, uint32_t parity) const {
+    return __all_sync(0xFFFFFFFFu, wait(bar, parity));
   }
   // Used while winding down: ignores the abort flag, still bounded.
   __device__ bool drain(uint64_t* bar, uint32_t parity) const {
@@ -553,7 +559,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
-    if (lane == 0) {
+    // The whole warp runs the loop and one elected lane issues the copies.
+    // (The same loop run by one lane alone took several times as many cycles
+    // per stage whenever the epilogue warps sharing its SM sub-partition were
+    // busy, and the stage time followed.)
+    {
+      const bool issuer = ptx::elect_one();
       const uint64_t pol_w = p.n_mt > 1 ? ptx::policy_evict_normal() : ptx::policy_evict_first();
       const uint64_t pol_h = ptx::policy_evict_last();
       uint32_t stage = 0, phase = 0, issued = 0;
@@ -563,8 +574,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto flush_h = [&]() {
         ptx::grid_dependency_wait();
         for (int i = 0; i < defer.n; ++i)
-          ptx::tma_load_2d(smem + size_t(defer.stage[i]) * p.stage_bytes, &tmap_h,
-                           &full_bar[defer.stage[i]], defer.kb[i] * kBlockK, defer.row[i], pol_h);
+          if (issuer)
+            ptx::tma_load_2d(smem + size_t(defer.stage[i]) * p.stage_bytes, &tmap_h,
+                             &full_bar[defer.stage[i]], defer.kb[i] * kBlockK, defer.row[i], pol_h);
         defer.n = 0;
         deferring = false;
       };
@@ -578,19 +590,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             int((uint32_t(vt + (p.vocab_offset >> 8)) * 5u) % uint32_t(p.n_kb));
         for (int kk = 0; kk < p.n_kb; ++kk) {
           const int kb = kk + k_start < p.n_kb ? kk + k_start : kk + k_start - p.n_kb;
-          if (!waiter.wait(&empty_bar[stage], phase ^ 1u)) {
+          if (!waiter.wait_warp(&empty_bar[stage], phase ^ 1u)) {
             ok = false;
             break;
           }
           uint8_t* sa = smem + size_t(stage) * p.stage_bytes;
-          ptx::mbar_arrive_expect_tx(&full_bar[stage], h_bytes + kSmemB);
-          ptx::tma_load_2d(sa + h_bytes, &tmap_w, &full_bar[stage], kb * kBlockK, vt * kBlockN,
-                           pol_w);
+          if (issuer) {
+            ptx::mbar_arrive_expect_tx(&full_bar[stage], h_bytes + kSmemB);
+            ptx::tma_load_2d(sa + h_bytes, &tmap_w, &full_bar[stage], kb * kBlockK, vt * kBlockN,
+                             pol_w);
+          }
           if (deferring) {
             defer.stage[defer.n] = stage;
             defer.kb[defer.n] = kb;
             defer.row[defer.n++] = mt * kBlockM;
-          } else {
+          } else if (issuer) {
             ptx::tma_load_2d(sa, &tmap_h, &full_bar[stage], kb * kBlockK, mt * kBlockM, pol_h);
           }
           ++issued;
@@ -612,42 +626,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
-    if (lane == 0) {
+    // Warp-wide like the producer; one elected lane issues the MMAs and
+    // commits.  Stage s's operand descriptors are stage 0's plus s times the
+    // stage size / 16 in the start-address field (shared-memory addresses stay
+    // below 256 KB, so the 14-bit field never carries), and a K step of 16
+    // bf16 (32 bytes) adds 2.
+    {
+      const bool issuer = ptx::elect_one();
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
+      const uint32_t s0 = ptx::smem_u32(smem);
+      const uint64_t desc_a0 = ptx::smem_desc_sw128(s0);
+      const uint64_t desc_b0 = ptx::smem_desc_sw128(s0 + h_bytes);
+      const uint32_t stage_units = p.stage_bytes >> 4;
       for (int unit = blockIdx.x; ok && unit < n_units; unit += gridDim.x) {
-        if (!waiter.wait(&tempty_bar[acc], acc_phase ^ 1u)) break;
+        if (!waiter.wait_warp(&tempty_bar[acc], acc_phase ^ 1u)) break;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * kBlockN;
         for (int kb = 0; kb < p.n_kb; ++kb) {
-          if (!waiter.wait(&full_bar[stage], phase)) {
+          if (!waiter.wait_warp(&full_bar[stage], phase)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
-          // A spans 128 rows; those past the H box read whatever follows it
-          // in shared memory and feed only accumulator rows that are never read.
-          const uint32_t sa = ptx::smem_u32(smem + size_t(stage) * p.stage_bytes);
-          const uint32_t sb = sa + h_bytes;
+          const uint64_t off = uint64_t(stage * stage_units);
+          if (issuer) {
 #pragma unroll
-          for (int k = 0; k < kBlockK / kUmmaK; ++k) {
-            ptx::mma_bf16(d_tmem, ptx::smem_desc_sw128(sa + k * kUmmaK * 2),
-                          ptx::smem_desc_sw128(sb + k * kUmmaK * 2), kIdesc,
-                          (kb | k) != 0 ? 1u : 0u);
+            for (int k = 0; k < kBlockK / kUmmaK; ++k)
+              ptx::mma_bf16(d_tmem, desc_a0 + off + uint64_t(2 * k),
+                            desc_b0 + off + uint64_t(2 * k), kIdesc, (kb | k) != 0 ? 1u : 0u);
+            ptx::mma_commit(&empty_bar[stage]);
           }
-          ptx::mma_commit(&empty_bar[stage]);
+          __syncwarp();
           if (++stage == p.n_stages) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        ptx::mma_commit(&tfull_bar[acc]);
+        if (issuer) ptx::mma_commit(&tfull_bar[acc]);
+        __syncwarp();
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
       }
       // All MMAs must be complete before tensor memory is released.
-      ptx::mma_commit(drain_bar);
+      if (issuer) ptx::mma_commit(drain_bar);
+      __syncwarp();
       waiter.drain(drain_bar, 0);
     }
     __syncwarp();
@@ -768,7 +792,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ---------------- TMA producer (both CTAs) ----------------
-    if (lane == 0) {
+    // Warp-wide, one elected lane issuing (as in stage1_kernel).
+    {
+      const bool issuer = ptx::elect_one();
       const uint64_t pol_w = n_mp > 1 ? ptx::policy_evict_normal() : ptx::policy_evict_first();
       const uint64_t pol_h = ptx::policy_evict_last();
       uint32_t stage = 0, phase = 0, issued = 0;
@@ -778,9 +804,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto flush_h = [&]() {
         ptx::grid_dependency_wait();
         for (int i = 0; i < defer.n; ++i)
-          ptx::tma_load_2d_pair(smem + size_t(defer.stage[i]) * kPairStageBytes, &tmap_h,
-                                ptx::cluster_addr(&full_bar[defer.stage[i]], 0),
-                                defer.kb[i] * kBlockK, defer.row[i], pol_h);
+          if (issuer)
+            ptx::tma_load_2d_pair(smem + size_t(defer.stage[i]) * kPairStageBytes, &tmap_h,
+                                  ptx::cluster_addr(&full_bar[defer.stage[i]], 0),
+                                  defer.kb[i] * kBlockK, defer.row[i], pol_h);
         defer.n = 0;
         deferring = false;
       };
@@ -795,19 +822,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int w_y = min(vt * kBlockN + rank * (kBlockN / 2), p.V - 1);
         for (int kk = 0; kk < p.n_kb; ++kk) {
           const int kb = kk + k_start < p.n_kb ? kk + k_start : kk + k_start - p.n_kb;
-          if (!waiter.wait(&empty_bar[stage], phase ^ 1u)) {
+          if (!waiter.wait_warp(&empty_bar[stage], phase ^ 1u)) {
             ok = false;
             break;
           }
           uint8_t* sa = smem + size_t(stage) * kPairStageBytes;
           const uint32_t full_addr = ptx::cluster_addr(&full_bar[stage], 0);
-          if (leader) ptx::mbar_arrive_expect_tx(&full_bar[stage], 2 * kPairStageBytes);
-          ptx::tma_load_2d_pair(sa + kPairSmemA, &tmap_w, full_addr, kb * kBlockK, w_y, pol_w);
+          if (issuer) {
+            if (leader) ptx::mbar_arrive_expect_tx(&full_bar[stage], 2 * kPairStageBytes);
+            ptx::tma_load_2d_pair(sa + kPairSmemA, &tmap_w, full_addr, kb * kBlockK, w_y, pol_w);
+          }
           if (deferring) {
             defer.stage[defer.n] = stage;
             defer.kb[defer.n] = kb;
             defer.row[defer.n++] = a_y;
-          } else {
+          } else if (issuer) {
             ptx::tma_load_2d_pair(sa, &tmap_h, full_addr, kb * kBlockK, a_y, pol_h);
           }
           ++issued;
@@ -831,39 +860,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ---------------- MMA issuer (leader CTA only) ----------------
-    if (lane == 0 && leader) {
+    // Warp-wide, one elected lane issuing (as in stage1_kernel).
+    if (leader) {
+      const bool issuer = ptx::elect_one();
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
+      const uint32_t s0 = ptx::smem_u32(smem);
+      const uint64_t desc_a0 = ptx::smem_desc_sw128(s0);
+      const uint64_t desc_b0 = ptx::smem_desc_sw128(s0 + kPairSmemA);
       for (int u = pair_id; ok && u < n_units; u += n_pairs) {
-        if (!waiter.wait(&tempty_bar[acc], acc_phase ^ 1u)) break;
+        if (!waiter.wait_warp(&tempty_bar[acc], acc_phase ^ 1u)) break;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * kBlockN;
         for (int kb = 0; kb < p.n_kb; ++kb) {
-          if (!waiter.wait(&full_bar[stage], phase)) {
+          if (!waiter.wait_warp(&full_bar[stage], phase)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after();
-          const uint32_t sa = ptx::smem_u32(smem + size_t(stage) * kPairStageBytes);
-          const uint32_t sb = sa + kPairSmemA;
+          const uint64_t off = uint64_t(stage * (kPairStageBytes >> 4));
+          if (issuer) {
 #pragma unroll
-          for (int k = 0; k < kBlockK / kUmmaK; ++k) {
-            ptx::mma_bf16_pair(d_tmem, ptx::smem_desc_sw128(sa + k * kUmmaK * 2),
-                               ptx::smem_desc_sw128(sb + k * kUmmaK * 2), kPairIdesc,
-                               (kb | k) != 0 ? 1u : 0u);
+            for (int k = 0; k < kBlockK / kUmmaK; ++k)
+              ptx::mma_bf16_pair(d_tmem, desc_a0 + off + uint64_t(2 * k),
+                                 desc_b0 + off + uint64_t(2 * k), kPairIdesc,
+                                 (kb | k) != 0 ? 1u : 0u);
+            ptx::mma_commit_pair_multicast(&empty_bar[stage], 0x3);
           }
-          ptx::mma_commit_pair_multicast(&empty_bar[stage], 0x3);
+          __syncwarp();
           if (++stage == kPairStages) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        ptx::mma_commit_pair_multicast(&tfull_bar[acc], 0x3);
+        if (issuer) ptx::mma_commit_pair_multicast(&tfull_bar[acc], 0x3);
+        __syncwarp();
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
       }
-      ptx::mma_commit_pair(drain_bar);
+      if (issuer) ptx::mma_commit_pair(drain_bar);
+      __syncwarp();
       waiter.drain(drain_bar, 0);
     }
     __syncwarp();

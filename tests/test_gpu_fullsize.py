@@ -103,6 +103,30 @@ def test_qwen3_8b_head(B):
         compare(p, dev, sample_rows(B, k=2, seed=step), offset=step, seed=0, W_bits=Wb)
 
 
+@pytest.mark.parametrize("B", [128, 512])
+def test_qwen3_8b_whole_batch_against_oracle(B):
+    """Every row of a production-size batch against the oracle: the Qwen3-8B
+    head with its per-row temperatures (10% greedy) and seeds, B = 128 on the
+    single-CTA kernel and B = 512 on the CTA-pair kernel.  The ids of the call
+    the benchmark times (no per-tile outputs) equal those of the call that
+    also writes them; then every row's id, and every tile's max, argmax and
+    log-sum-exp, go through the parity gate."""
+    W, Wb = weights("qwen3-8b")
+    V = W.shape[0]
+    p = make_problem(B, W.shape[1], V, T="row-uniform", per_row_seeds=True, seed=700 + B, W=W)
+    out = torch.empty(B, dtype=torch.int64, device="cuda")
+    ws = torch.zeros(fs.fs_workspace_size(B, V), dtype=torch.uint8, device="cuda")
+    fs.fs_sample(p["H"], W, temperature=p["temperature"], seeds=p["seeds"], offset=17,
+                 out_idx=out, workspace=ws)
+    dev = run_device(p, seed=0, offset=17, lse=True)
+    assert np.array_equal(out.cpu().numpy(), dev["idx"])
+    whole_batch_properties(p, dev, V)
+    st = compare(p, dev, list(range(B)), seed=0, offset=17, W_bits=Wb)
+    assert st["rows"] == B and st["tiles"] == B * fs.fs_num_tiles(V), st
+    # nearly every row is decided by a gap the gate resolves
+    assert st["rows_gated"] >= 0.9 * B, st
+
+
 def test_llama3_8b_masked_head():
     W, Wb = weights("llama3-8b-mask")
     B = 128
