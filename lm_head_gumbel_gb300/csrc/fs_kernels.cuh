@@ -476,6 +476,8 @@ enum : int {
 __host__ __device__ constexpr int topk_cap(int mode) {
   return mode == kModeTop4 ? 4 : mode == kModeTop16 ? 16 : 1;
 }
+template <int kMode>
+constexpr bool kTopkMode = kMode == kModeTop4 || kMode == kModeTop16;
 
 // Per-thread epilogue state carried across units: the running top-K list in
 // the top-K modes, nothing otherwise.
@@ -551,8 +553,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // A kernel launched after this one as a programmatic dependent may be
   // scheduled from now on, on whatever SM resources are free (for another
   // sampling call: the SMs this grid's blocks leave); it must wait for this
-  // grid to complete before it reads anything this grid writes.
-  ptx::grid_launch_dependents();
+  // grid to complete before it reads anything this grid writes.  The top-K
+  // modes let their dependent (the list reduction, which can do nothing
+  // before this grid ends) be scheduled only as each block finishes.
+  if constexpr (!kTopkMode<kMode>) ptx::grid_launch_dependents();
   const uint32_t tmem_base = *tmem_holder;
   const Waiter waiter{abort_flag, p.wait_limit_ns};
   const uint32_t h_bytes = p.h_box_rows * 128u;  // the H box; the W slice follows it
@@ -714,6 +718,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tmem_dealloc(tmem_base, kTmemCols);
   }
   finish_rows(p);
+  if constexpr (kTopkMode<kMode>) ptx::grid_launch_dependents();
 }
 
 // ---------------------------------------------------------------------------
@@ -786,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::cluster_sync();  // both CTAs' barriers exist before either uses the other's
   ptx::tc_fence_after();
-  ptx::grid_launch_dependents();  // as in stage1_kernel
+  if constexpr (!kTopkMode<kMode>) ptx::grid_launch_dependents();  // as in stage1_kernel
   const uint32_t tmem_base = *tmem_holder;
   const Waiter waiter{abort_flag, p.wait_limit_ns};
 
@@ -949,6 +954,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   ptx::cluster_sync();
   finish_rows(p);
+  if constexpr (kTopkMode<kMode>) ptx::grid_launch_dependents();
 }
 
 // Diagnostic: the bounded wait of the sampling kernels, on an mbarrier that no

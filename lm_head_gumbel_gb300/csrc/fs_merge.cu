@@ -211,22 +211,22 @@ __device__ __forceinline__ void warp_select(float (&ls)[KC], int32_t (&li)[KC], 
   }
 }
 
-// Each row's K best of its candidate lists (Gumbel-top-k: K draws without
-// replacement, in draw order).  One block per row.  Every slot holds a list
-// sorted best first (an empty list starts with id -1).  A thread reads the
-// heads of 8 of its slots at once, loads a whole list (16-byte loads) only
-// when its head makes the thread's own KC-best list, and merges it by a
-// bitonic network.  Then each warp picks its K best by shuffles, and warp 0
-// picks the row's K best from the warps' lists.
+// Every list of one row merged into the row's K best (the fallback of
+// topk_reduce_kernel below).  Every slot holds a list sorted best first (an
+// empty list starts with id -1).  A thread reads the heads of 8 of its slots
+// at once, loads a whole list (16-byte loads) only when its head makes the
+// thread's own KC-best list, and merges it by a bitonic network.  Then each
+// warp picks its K best by shuffles, and warp 0 picks the row's K best from
+// the warps' lists.
 template <int KC>
-__global__ void __launch_bounds__(kTopkThreads)
-    topk_reduce_kernel(const float* __restrict__ cand_score,
-                       const int32_t* __restrict__ cand_idx, int32_t n_tiles, int32_t K,
-                       int64_t* __restrict__ out_idx, float* __restrict__ out_score) {
+__device__ __noinline__ void merge_all_lists(const float* __restrict__ cand_score,
+                                             const int32_t* __restrict__ cand_idx,
+                                             int32_t n_tiles, int32_t K,
+                                             int64_t* __restrict__ out_idx,
+                                             float* __restrict__ out_score, int row) {
   static_assert(KC % 4 == 0, "lists are read 4 entries at a time");
   constexpr int kWarps = kTopkThreads / 32;
   constexpr int kGroup = 8;
-  const int row = blockIdx.x;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t base = int64_t(row) * n_tiles * KC;
   float ls[KC];
@@ -300,18 +300,212 @@ __global__ void __launch_bounds__(kTopkThreads)
   });
 }
 
+constexpr int kSurvivorCap = 256;
+
+// Each row's K best of its candidate lists (Gumbel-top-k: K draws without
+// replacement, in draw order).  One block per row.  Two lower bounds of the
+// row's K-th best score: the K-th best of the threads' best list heads (K
+// distinct entries reach it), and the largest K-th entry of a list (that list
+// alone holds K entries reaching it).  Only entries reaching tau, the larger
+// bound, can be among the row's K best, and only lists whose head reaches tau
+// hold any: the block gathers those entries (at the Qwen3-8B head, K and a
+// few more) into shared memory and ranks them (score descending, id
+// ascending).  A row where more than kSurvivorCap entries reach tau (many
+// equal scores, or fewer than K entries in all) merges all its lists
+// instead.  Launched as a programmatic dependent of the stage-1 kernel, which
+// lets it start as its blocks finish; it reads the lists only after the
+// stage-1 grid has completed.
+template <int KC>
+__global__ void __launch_bounds__(kTopkThreads)
+    topk_reduce_kernel(const float* __restrict__ cand_score,
+                       const int32_t* __restrict__ cand_idx, int32_t n_tiles, int32_t K,
+                       int64_t* __restrict__ out_idx, float* __restrict__ out_score) {
+  constexpr int kWarps = kTopkThreads / 32;
+  __shared__ float s_part[kWarps];
+  __shared__ int s_n;
+  __shared__ float s_tau_head;
+  __shared__ float s_hs[kTopkThreads];
+  __shared__ int32_t s_hi[kTopkThreads];
+  __shared__ float s_score[kSurvivorCap];
+  __shared__ int32_t s_id[kSurvivorCap];
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the stage-1 grid is complete
+  const int row = blockIdx.x;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t base = int64_t(row) * n_tiles * KC;
+  if (threadIdx.x == 0) {
+    s_n = 0;
+    s_tau_head = -INFINITY;
+  }
+  __syncthreads();
+  // Each thread's best list head, and the largest K-th entry of a list: the
+  // heads and K-th entries of kGroup slots are loaded at once.
+  constexpr int kGroup = 8;
+  float tau = -INFINITY;
+  float hb = -INFINITY;
+  int32_t hbi = -1;
+  int32_t hid0[kGroup];
+  float hs0[kGroup];
+  for (int t0 = threadIdx.x; t0 < n_tiles; t0 += kTopkThreads * kGroup) {
+    int32_t hid[kGroup];
+    float hs[kGroup], hk[kGroup];
+#pragma unroll
+    for (int g = 0; g < kGroup; ++g) {
+      const int t = t0 + g * kTopkThreads;
+      hid[g] = -1;
+      hs[g] = hk[g] = -INFINITY;
+      if (t < n_tiles) {
+        const int64_t o = base + int64_t(t) * KC;
+        hid[g] = cand_idx[o];
+        hs[g] = cand_score[o];
+        hk[g] = cand_score[o + (K - 1)];
+      }
+    }
+    if (t0 == int(threadIdx.x)) {
+#pragma unroll
+      for (int g = 0; g < kGroup; ++g) {
+        hid0[g] = hid[g];
+        hs0[g] = hs[g];
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < kGroup; ++g) {
+      if (hid[g] < 0) continue;
+      tau = fmaxf(tau, hk[g]);
+      if (precedes(hs[g], hid[g], hb, hbi)) {
+        hb = hs[g];
+        hbi = hid[g];
+      }
+    }
+  }
+  if (int(threadIdx.x) >= n_tiles) {
+#pragma unroll
+    for (int g = 0; g < kGroup; ++g) {
+      hid0[g] = -1;
+      hs0[g] = -INFINITY;
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) tau = fmaxf(tau, __shfl_xor_sync(0xFFFFFFFFu, tau, off));
+  if (lane == 0) s_part[warp] = tau;
+  // Sort the threads' best heads, best first (bitonic network: exchanges
+  // within a warp by shuffles, across warps through shared memory); the K-th
+  // of them is reached by K distinct entries.
+#pragma unroll
+  for (int k = 2; k <= kTopkThreads; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      float os;
+      int32_t oi;
+      if (j >= 32) {
+        __syncthreads();
+        s_hs[threadIdx.x] = hb;
+        s_hi[threadIdx.x] = hbi;
+        __syncthreads();
+        os = s_hs[threadIdx.x ^ j];
+        oi = s_hi[threadIdx.x ^ j];
+      } else {
+        os = __shfl_xor_sync(0xFFFFFFFFu, hb, j);
+        oi = __shfl_xor_sync(0xFFFFFFFFu, hbi, j);
+      }
+      const bool lower = (threadIdx.x & j) == 0;
+      const bool best_first = (threadIdx.x & k) == 0;
+      const bool other_better = precedes(os, oi, hb, hbi);
+      if (other_better == (lower == best_first)) {
+        hb = os;
+        hbi = oi;
+      }
+    }
+  }
+  if (threadIdx.x == K - 1) s_tau_head = hbi >= 0 ? hb : -INFINITY;
+  __syncthreads();
+  tau = s_tau_head;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) tau = fmaxf(tau, s_part[w]);
+  // The entries reaching tau, from the lists whose head reaches it (the heads
+  // of the first group are still in registers).
+  for (int t0 = threadIdx.x; t0 < n_tiles; t0 += kTopkThreads * kGroup) {
+    if (t0 != int(threadIdx.x)) {
+#pragma unroll
+      for (int g = 0; g < kGroup; ++g) {
+        const int t = t0 + g * kTopkThreads;
+        hid0[g] = -1;
+        hs0[g] = -INFINITY;
+        if (t < n_tiles) {
+          hid0[g] = cand_idx[base + int64_t(t) * KC];
+          hs0[g] = cand_score[base + int64_t(t) * KC];
+        }
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < kGroup; ++g) {
+      if (hid0[g] < 0 || !(hs0[g] >= tau)) continue;
+      const int64_t o = base + int64_t(t0 + g * kTopkThreads) * KC;
+      const float4* s4 = reinterpret_cast<const float4*>(cand_score + o);
+      const int4* i4 = reinterpret_cast<const int4*>(cand_idx + o);
+#pragma unroll
+      for (int q4 = 0; q4 < KC / 4; ++q4) {
+        const float4 a4 = s4[q4];
+        const int4 b4 = i4[q4];
+        const float cs[4] = {a4.x, a4.y, a4.z, a4.w};
+        const int32_t ci[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (ci[q] >= 0 && cs[q] >= tau) {  // lists are sorted, so these come first
+            const int pos = atomicAdd(&s_n, 1);
+            if (pos < kSurvivorCap) {
+              s_score[pos] = cs[q];
+              s_id[pos] = ci[q];
+            }
+          }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  const int n = s_n;
+  if (n > kSurvivorCap) {  // block-uniform
+    merge_all_lists<KC>(cand_score, cand_idx, n_tiles, K, out_idx, out_score, row);
+    return;
+  }
+  for (int i = threadIdx.x; i < n; i += kTopkThreads) {
+    const float si = s_score[i];
+    const int32_t ii = s_id[i];
+    int rank = 0;
+    for (int j = 0; j < n; ++j) rank += precedes(s_score[j], s_id[j], si, ii) ? 1 : 0;
+    if (rank < K) {
+      out_idx[int64_t(row) * K + rank] = ii;
+      if (out_score != nullptr) out_score[int64_t(row) * K + rank] = si;
+    }
+  }
+  for (int r = n + threadIdx.x; r < K; r += kTopkThreads) {  // fewer candidates than K
+    out_idx[int64_t(row) * K + r] = -1;
+    if (out_score != nullptr) out_score[int64_t(row) * K + r] = -INFINITY;
+  }
+}
+
 }  // namespace
 
 fs_status launch_topk_reduce(const float* cand_score, const int32_t* cand_idx, int64_t B,
                              int64_t n_tiles, int64_t cap, int64_t K, int64_t* out_idx,
                              float* out_score, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(B), 1, 1);
+  cfg.blockDim = dim3(kTopkThreads, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e;
   if (cap == 4)
-    topk_reduce_kernel<4><<<unsigned(B), kTopkThreads, 0, stream>>>(
-        cand_score, cand_idx, int32_t(n_tiles), int32_t(K), out_idx, out_score);
+    e = cudaLaunchKernelEx(&cfg, topk_reduce_kernel<4>, cand_score, cand_idx, int32_t(n_tiles),
+                           int32_t(K), out_idx, out_score);
   else
-    topk_reduce_kernel<16><<<unsigned(B), kTopkThreads, 0, stream>>>(
-        cand_score, cand_idx, int32_t(n_tiles), int32_t(K), out_idx, out_score);
-  return cudaGetLastError() == cudaSuccess ? FS_OK : FS_ERR_CUDA;
+    e = cudaLaunchKernelEx(&cfg, topk_reduce_kernel<16>, cand_score, cand_idx, int32_t(n_tiles),
+                           int32_t(K), out_idx, out_score);
+  if (e != cudaSuccess) cudaGetLastError();
+  return e == cudaSuccess ? FS_OK : FS_ERR_CUDA;
 }
 
 fs_status launch_row_lse(const float* tile_lse, const float* temperature, int64_t B,

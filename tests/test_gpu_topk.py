@@ -183,3 +183,20 @@ def test_topk_full_size_head(B, K):
     assert np.all((idx >= 0) & (idx < w.V))
     rows = [0, B // 3, B - 1]
     assert check_against_oracle(p, K, idx, score, rows=rows, offset=2) >= len(rows) * K * 0.6
+
+
+@pytest.mark.parametrize("K", [4, 16])
+def test_topk_equal_scores_take_the_lowest_ids(K):
+    """Every logit of a row equal (all W rows the same): greedy rows tie on
+    every id, so their K draws are ids 0..K-1 (the tie rule), and so many
+    entries reach the reduction's threshold that it merges every list; sampled
+    rows of the same call (distinct noise, no ties) still match the oracle."""
+    B, d, V = 8, 64, 40000
+    p = make_problem(B, d, V, T=1.0, seed=88)
+    p["W"] = p["W"][:1].expand(V, d).contiguous()
+    p["temperature"][:4] = 0.0
+    idx, score = device_topk(p, K, seed=5, offset=2)
+    for b in range(4):
+        assert np.array_equal(idx[b], np.arange(K)), (b, idx[b])
+        assert np.all(score[b] == score[b, 0])
+    check_against_oracle(p, K, idx, score, rows=list(range(4, B)), seed=5, offset=2)
