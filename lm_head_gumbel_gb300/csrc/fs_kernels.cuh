@@ -502,6 +502,147 @@ __device__ __forceinline__ void epilogue_finish(const Stage1Params& p, EpilogueS
   if constexpr (kMode == kModeTop4 || kMode == kModeTop16) topk_flush<topk_cap(kMode)>(p, st);
 }
 
+// The last unit of a CTA in the sampling mode, when the batch has at most
+// kSpreadRows rows.  Nothing overlaps the epilogue of a CTA's last unit, and
+// with few rows only one or two lane quadrants hold rows, so only the two
+// warps of each such quadrant would work through 128 ids a row each.
+// Instead every epilogue warp copies its rows' logits out of tensor memory
+// into the (now idle) ring of shared memory, and the eight warps then take
+// one 32-id chunk of one row each (two with more than 32 rows); a second pass
+// merges each tile's four chunks in id order.  The per-chunk arithmetic is
+// the same as the other path's, so the samples and tile outputs are
+// bit-identical to it.
+constexpr int kSpreadRows = 64;
+constexpr uint32_t kSpreadRowBytes = kBlockN * 4 + 16;  // a row of fp32 logits + 16 B pad
+constexpr uint32_t kSpreadResOffset = kSpreadRows * kSpreadRowBytes;
+static_assert(kSpreadResOffset + kSpreadRows * 8 * 8 <= kRingBytes, "spread buffers fit the ring");
+
+struct ChunkBest {
+  float best;  // base-2 score (greedy rows: the logit)
+  int32_t j;   // its position in the chunk, -1 if none
+};
+
+__device__ __forceinline__ void spread_stage(uint8_t* smem, uint32_t taddr, int r, int col0) {
+  uint8_t* dst = smem + size_t(r) * kSpreadRowBytes + size_t(col0) * 4;
+#pragma unroll 1
+  for (int c = 0; c < kTileV / 32; ++c) {
+    uint32_t v[32];
+    ptx::tmem_ld_32x32b_x32(taddr + uint32_t(c * 32), v);
+    ptx::tmem_wait_ld();
+    uint4* d4 = reinterpret_cast<uint4*>(dst + c * 128);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) d4[q] = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+  }
+}
+
+// One 32-id chunk (row r of the unit, ids vt*256 + 32c ..) from the staged
+// logits: its best score and position, as in epilogue_tile.  `valid` lanes
+// only; every lane of the warp takes part in the mask vote.
+__device__ __forceinline__ ChunkBest spread_chunk(const Stage1Params& p, const uint8_t* smem,
+                                                  int vt, int r, int c, bool valid) {
+  ChunkBest out{-INFINITY, -1};
+  const int v0 = vt * kBlockN + c * 32;
+  float T = 1.0f;
+  uint64_t seed = p.seed;
+  uint32_t allow = 0u;
+  if (valid) {
+    if (p.temperature) T = p.temperature[r];
+    if (p.seeds) seed = p.seeds[r];
+    allow = p.mask ? p.mask[int64_t(r) * p.mask_ld + (v0 >> 5)] : 0xFFFFFFFFu;
+    const int n_in = p.V - v0;
+    if (n_in < 32) allow &= (n_in <= 0) ? 0u : ((1u << n_in) - 1u);
+  }
+  const bool unmasked = __all_sync(0xFFFFFFFFu, allow == 0xFFFFFFFFu);
+  if (!valid) return out;
+  uint32_t v[32];
+  const uint4* s4 = reinterpret_cast<const uint4*>(smem + size_t(r) * kSpreadRowBytes + c * 128);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const uint4 x = s4[q];
+    v[4 * q] = x.x, v[4 * q + 1] = x.y, v[4 * q + 2] = x.z, v[4 * q + 3] = x.w;
+  }
+  const bool greedy = !(T > 0.0f) || isinf(T);
+  if (greedy) {
+    if (unmasked)
+      greedy_chunk<false>(v, allow, out.best, out.j);
+    else
+      greedy_chunk<true>(v, allow, out.best, out.j);
+  } else {
+    const float scale2 = kLog2e / T;
+    const PhiloxSchedule ks(seed);
+    const uint32_t ctr0 = static_cast<uint32_t>((p.vocab_offset + v0) >> 2);
+    const uint32_t ctr_row = static_cast<uint32_t>(r);
+    const uint32_t ctr_lo = static_cast<uint32_t>(p.offset);
+    const uint32_t ctr_hi = static_cast<uint32_t>(p.offset >> 32);
+    if (unmasked)
+      sample_chunk<false>(v, allow, scale2, ctr0, ctr_row, ctr_lo, ctr_hi, ks, out.best, out.j);
+    else
+      sample_chunk<true>(v, allow, scale2, ctr0, ctr_row, ctr_lo, ctr_hi, ks, out.best, out.j);
+  }
+  return out;
+}
+
+// The epilogue of the spread last unit, run by the eight epilogue warps once
+// the unit's accumulator is full.  Returns false if a wait timed out.
+__device__ __forceinline__ bool spread_last_unit(const Stage1Params& p, uint8_t* smem,
+                                                 uint32_t tmem_acc, int vt, int quad, int half,
+                                                 int lane, int e, const Waiter& waiter,
+                                                 uint64_t* staged_bar, uint64_t* chunks_bar) {
+  const int rows = p.B;  // one batch block of at most kSpreadRows rows
+  if (quad * 32 < rows)
+    spread_stage(smem, tmem_acc + (uint32_t(quad * 32) << 16) + uint32_t(half * kTileV),
+                 quad * 32 + lane, half * kTileV);
+  __syncwarp();
+  int ok = 1;
+  if (lane == 0) {
+    ptx::mbar_arrive(staged_bar);
+    ok = waiter.wait(staged_bar, 0) ? 1 : 0;
+  }
+  if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) return false;
+  // Chunk k: row (k % 32) + 32 (k / 256), chunk (k / 32) % 8, so the 32 lanes
+  // of a warp read 32 rows of one chunk (no shared-memory bank conflicts).
+  ChunkBest* res = reinterpret_cast<ChunkBest*>(smem + kSpreadResOffset);
+  const int n_items = ((rows + 31) / 32) * 32 * 8;
+  for (int k0 = e * 32; k0 < n_items; k0 += kEpiWarps * 32) {
+    const int k = k0 + lane;
+    const int r = (k & 31) + ((k >> 8) << 5), c = (k >> 5) & 7;
+    const bool valid = r < rows && vt * 2 + (c >> 2) < p.n_tiles;
+    const ChunkBest b = spread_chunk(p, smem, vt, r, c, valid);
+    if (valid) res[r * 8 + c] = b;
+  }
+  __syncwarp();
+  if (lane == 0) {
+    ptx::mbar_arrive(chunks_bar);
+    ok = waiter.wait(chunks_bar, 0) ? 1 : 0;
+  }
+  if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) return false;
+  // Each (row, tile): its four chunks in id order, as epilogue_tile.
+  for (int k = e * 32 + lane; k < rows * 2; k += kEpiWarps * 32) {
+    const int r = k >> 1, h = k & 1, tile = vt * 2 + h;
+    if (tile >= p.n_tiles) continue;
+    const float T = p.temperature ? p.temperature[r] : 1.0f;
+    const bool greedy = !(T > 0.0f) || isinf(T);
+    float best = -INFINITY;
+    int32_t best_idx = -1;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const ChunkBest b = res[r * 8 + h * 4 + c];
+      if (b.j >= 0 && b.best > best) {
+        best = b.best;
+        best_idx = p.vocab_offset + tile * kTileV + c * 32 + b.j;
+      }
+    }
+    const float m = (greedy || best_idx < 0) ? best : kLn2 * (best - kLog2Ln2);
+    if (p.out_idx != nullptr && best_idx >= 0) atomicMax(p.row_keys + r, pack_key(m, best_idx));
+    if (p.tile_max != nullptr) {
+      const int64_t o = int64_t(r) * p.n_tiles + tile;
+      p.tile_max[o] = m;
+      p.tile_idx[o] = best_idx;
+    }
+  }
+  return true;
+}
+
 // Single-CTA stage 1: a unit is (vocabulary block vt of 256 ids, batch block mt
 // of 128 rows), computed by one CTA with M = 128, N = 256 MMAs; units are
 // ordered vocabulary-major so the batch blocks of one vocabulary block run on
@@ -518,7 +659,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tfull_bar = empty_bar + kMaxStages;
   uint64_t* tempty_bar = tfull_bar + 2;
   uint64_t* drain_bar = tempty_bar + 2;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain_bar + 1);
+  uint64_t* staged_bar = drain_bar + 1;  // the spread last unit (spread_last_unit)
+  uint64_t* chunks_bar = staged_bar + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(chunks_bar + 1);
   volatile uint32_t* abort_flag = tmem_holder + 1;
 
   const int warp = threadIdx.x >> 5;
@@ -536,6 +679,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&tempty_bar[a], kEpiWarps);
     }
     ptx::mbar_init(drain_bar, 1);
+    ptx::mbar_init(staged_bar, kEpiWarps);
+    ptx::mbar_init(chunks_bar, kEpiWarps);
     *abort_flag = 0u;
     ptx::fence_barrier_init();
   }
@@ -694,6 +839,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok) break;
       ptx::tc_fence_after();
+      if (kMode == kModeSample && p.B <= kSpreadRows && unit + int(gridDim.x) >= n_units) {
+        // The CTA's last unit, spread over all epilogue warps (then done).
+        spread_last_unit(p, smem, tmem_base + acc * kBlockN, vt, quad, half, lane, e, waiter,
+                         staged_bar, chunks_bar);
+        break;
+      }
       const int row0 = mt * kBlockM + quad * 32;
       const int tile = vt * 2 + half;
       if (row0 < p.B && tile < p.n_tiles) {
