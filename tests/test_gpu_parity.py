@@ -172,6 +172,24 @@ def test_rows_do_not_depend_on_the_batch(V):
     assert np.array_equal(runs[384]["tile_max"][:256], runs[256]["tile_max"])
 
 
+@pytest.mark.parametrize("B", [1, 5, 32, 40, 64])
+def test_spread_last_unit_is_bit_identical(B):
+    """In the sampling mode, batches of at most 64 rows spread each CTA's last
+    unit over all epilogue warps (through shared memory); a batch of 128 rows
+    does not.  The same rows inside both must give bit-identical samples and
+    per-tile maxima and argmaxes (masks, greedy rows and per-row seeds
+    included), and both must match the oracle."""
+    big = make_problem(128, 264, 5000, T="row-uniform", per_row_seeds=True, mask_frac=0.05,
+                       seed=120)
+    ref = run_device(big, seed=9, offset=4, lse=False)
+    sub = {k: (None if t is None else t[:B].contiguous()) if k != "W" else t
+           for k, t in big.items()}
+    got = run_device(sub, seed=9, offset=4, lse=False)
+    for k in ("idx", "tile_max", "tile_idx"):
+        assert np.array_equal(got[k], ref[k][:B]), k
+    compare(sub, got, seed=9, offset=4, scores=True)
+
+
 def test_tiny_temperature_is_effectively_greedy():
     """T = 1e-4 (l/T ~ 1e5, far from fp32 overflow): the sample is the argmax
     of the logits wherever the logit gap is clearly wider than the noise's
