@@ -97,3 +97,19 @@ def test_workload_descriptions_name_the_configuration():
     assert "d=4096" in s and "V=151936" in s and "B=64" in s and "per-row seeds" in s
     s = bench.describe(wl.WORKLOADS["llama3-8b-mask"], 128)
     assert "mask" in s and "x4" in s and "LSE" in s
+
+
+def test_default_run_times_every_workload():
+    """The default run's headline head plus its other workloads cover every
+    workload of the benchmark set, each with its own batch sizes and a
+    description and L2 note taken from its definition."""
+    from lm_head_gumbel_gb300 import workloads as wl
+    assert set(bench.OTHER_WORKLOADS) == set(wl.WORKLOADS)
+    for name in bench.OTHER_WORKLOADS:
+        w = wl.WORKLOADS[name]
+        text = bench.describe(w, "/".join(str(b) for b in w.batches))
+        assert f"d={w.d}" in text and f"V={w.V}" in text
+        note = bench.l2_note(w.V, w.d)
+        assert ("fits in L2" in note) == (w.V * w.d * 2 <= bench.L2_BYTES)
+    assert "fits in L2" in bench.l2_note(4096, 256)       # the tiny head: warm
+    assert "exceed L2" in bench.l2_note(151936, 4096)     # the Qwen3-8B head: cold
