@@ -127,6 +127,32 @@ def test_qwen3_8b_whole_batch_against_oracle(B):
     assert st["rows_gated"] >= 0.9 * B, st
 
 
+def test_large_vocab_whole_batch_against_oracle():
+    """Every row and tile of the large-vocabulary head (d=5120, V=262144) at
+    B = 512 against the oracle: the CTA-pair kernel in its tile-LSE mode, at
+    the size the benchmark times."""
+    W, Wb = weights("large-vocab")
+    V, B = W.shape[0], 512
+    p = make_problem(B, W.shape[1], V, T=0.8, seed=900, W=W)
+    dev = run_device(p, seed=77, offset=5, lse=True)
+    whole_batch_properties(p, dev, V)
+    st = compare(p, dev, list(range(B)), seed=77, offset=5, W_bits=Wb)
+    assert st["rows"] == B and st["tiles"] == B * fs.fs_num_tiles(V), st
+    assert st["rows_gated"] >= 0.9 * B and st["max_abs_tile_lse"] < 2e-3, st
+
+
+def test_qwen3_1_7b_whole_batch_against_oracle():
+    """Every row and tile of the Qwen3-1.7B head (d=2048) at B = 256 (the
+    CTA-pair kernel, 32 K slices a unit) against the oracle."""
+    W, Wb = weights("qwen3-1.7b")
+    V, B = W.shape[0], 256
+    p = make_problem(B, W.shape[1], V, T=0.7, seed=901, W=W)
+    dev = run_device(p, seed=2024, offset=3, lse=False)
+    whole_batch_properties(p, dev, V)
+    st = compare(p, dev, list(range(B)), seed=2024, offset=3, W_bits=Wb)
+    assert st["rows"] == B and st["rows_gated"] >= 0.9 * B, st
+
+
 def test_llama3_8b_masked_head():
     W, Wb = weights("llama3-8b-mask")
     B = 128
