@@ -205,11 +205,69 @@ __device__ __forceinline__ void greedy_chunk(const uint32_t (&r)[32], uint32_t a
   }
 }
 
+// sample_chunk with the chunk's noise q = log2(-log2 u) already made
+// (noise_ahead): the same sums in the same order, so the same result.
+template <bool kMasked>
+__device__ __forceinline__ void sample_chunk_pre(const uint32_t (&r)[32], const uint32_t (&q)[32],
+                                                 uint32_t allow, float scale2, float& best2,
+                                                 int& best_j) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const float s2 = fmaf(__uint_as_float(r[j]), scale2, -__uint_as_float(q[j]));
+    if ((!kMasked || ((allow >> j) & 1u)) && s2 > best2) {
+      best2 = s2;
+      best_j = j;
+    }
+  }
+}
+
+// The noise of a CTA's last unit, made before its logits exist.  Nothing
+// overlaps the epilogue of a CTA's last unit, but the noise does not depend on
+// the logits: while the unit's W slices stream in, each epilogue warp (idle
+// once the unit before is done) writes q = log2(-log2 u) for its 32 rows and
+// 128 ids into its own lanes and columns of the other accumulator buffer,
+// which no MMA writes any more.  The last epilogue then reads it beside the
+// logits.  A warp whose rows are all greedy or past the batch writes nothing.
+__device__ __forceinline__ void noise_ahead(const Stage1Params& p, uint32_t ntaddr, int row,
+                                            int tile) {
+  const bool valid_row = row < p.B;
+  float T = 1.0f;
+  uint64_t seed = p.seed;
+  if (valid_row) {
+    if (p.temperature) T = p.temperature[row];
+    if (p.seeds) seed = p.seeds[row];
+  }
+  const bool sampled = valid_row && T > 0.0f && !isinf(T);
+  if (!__any_sync(0xFFFFFFFFu, sampled)) return;
+  // Every lane makes noise (the unused lanes' too), so the warp stays converged.
+  const PhiloxSchedule ks(seed);
+  const uint32_t ctr_row = static_cast<uint32_t>(row);
+  const uint32_t ctr_lo = static_cast<uint32_t>(p.offset);
+  const uint32_t ctr_hi = static_cast<uint32_t>(p.offset >> 32);
+#pragma unroll 1
+  for (int c = 0; c < kTileV / 32; ++c) {
+    const uint32_t ctr0 = static_cast<uint32_t>((p.vocab_offset + tile * kTileV + c * 32) >> 2);
+    uint32_t q[32];
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      const uint4 rnd = philox4x32_10(make_uint4(ctr0 + g, ctr_row, ctr_lo, ctr_hi), ks);
+      q[4 * g + 0] = __float_as_uint(gumbel_log2_from_word(rnd.x));
+      q[4 * g + 1] = __float_as_uint(gumbel_log2_from_word(rnd.y));
+      q[4 * g + 2] = __float_as_uint(gumbel_log2_from_word(rnd.z));
+      q[4 * g + 3] = __float_as_uint(gumbel_log2_from_word(rnd.w));
+    }
+    ptx::tmem_st_32x32b_x32(ntaddr + uint32_t(c * 32), q);
+  }
+  ptx::tmem_wait_st();
+}
+
 // One thread, one batch row, one 128-id output tile: read the logits from
 // tensor memory 32 columns at a time and reduce them to (m_t, i_t[, L_t]).
-template <bool kWantLse>
+// With kPreNoise the noise is read from tensor memory at ntaddr (noise_ahead)
+// instead of being made here.
+template <bool kWantLse, bool kPreNoise>
 __device__ __forceinline__ void epilogue_tile(const Stage1Params& p, uint32_t taddr, int row,
-                                              int tile) {
+                                              int tile, uint32_t ntaddr) {
   const bool valid_row = row < p.B;
   float T = 1.0f;
   uint64_t seed = p.seed;
@@ -225,6 +283,8 @@ __device__ __forceinline__ void epilogue_tile(const Stage1Params& p, uint32_t ta
   const uint32_t ctr_row = static_cast<uint32_t>(row);
   const uint32_t ctr_lo = static_cast<uint32_t>(p.offset);
   const uint32_t ctr_hi = static_cast<uint32_t>(p.offset >> 32);
+  // noise_ahead wrote noise only for warps with a sampled row.
+  const bool load_noise = kPreNoise && __any_sync(0xFFFFFFFFu, valid_row && !greedy);
 
   float best = -INFINITY;  // greedy: max l; sampling: max s2
   int32_t best_idx = -1;
@@ -234,7 +294,9 @@ __device__ __forceinline__ void epilogue_tile(const Stage1Params& p, uint32_t ta
 #pragma unroll 1
   for (int c = 0; c < kTileV / 32; ++c) {
     uint32_t r[32];
+    uint32_t qn[32];
     ptx::tmem_ld_32x32b_x32(taddr + uint32_t(c * 32), r);
+    if (load_noise) ptx::tmem_ld_32x32b_x32(ntaddr + uint32_t(c * 32), qn);
     ptx::tmem_wait_ld();
     const int v0 = v_tile + c * 32;
     uint32_t allow = 0xFFFFFFFFu;
@@ -253,6 +315,11 @@ __device__ __forceinline__ void epilogue_tile(const Stage1Params& p, uint32_t ta
         greedy_chunk<false>(r, allow, best, best_j);
       else
         greedy_chunk<true>(r, allow, best, best_j);
+    } else if (kPreNoise) {
+      if (unmasked)
+        sample_chunk_pre<false>(r, qn, allow, scale2, best, best_j);
+      else
+        sample_chunk_pre<true>(r, qn, allow, scale2, best, best_j);
     } else {
       const uint32_t ctr0 = static_cast<uint32_t>((p.vocab_offset + v0) >> 2);
       if (unmasked)
@@ -487,11 +554,15 @@ using EpilogueState =
     typename std::conditional<(kMode == kModeTop4 || kMode == kModeTop16),
                               TopKState<topk_cap(kMode)>, NoState>::type;
 
-template <int kMode>
+// One unit's epilogue for one thread; with kPreNoise (sampling modes only)
+// the noise is read from tensor memory at ntaddr (noise_ahead) instead of
+// being made.
+template <int kMode, bool kPreNoise>
 __device__ __forceinline__ void epilogue_unit(const Stage1Params& p, uint32_t taddr, int row,
-                                              int tile, EpilogueState<kMode>& st) {
+                                              int tile, EpilogueState<kMode>& st,
+                                              uint32_t ntaddr) {
   if constexpr (kMode == kModeSample || kMode == kModeLse)
-    epilogue_tile<kMode == kModeLse>(p, taddr, row, tile);
+    epilogue_tile<kMode == kModeLse, kPreNoise>(p, taddr, row, tile, ntaddr);
   else
     epilogue_tile_topk<topk_cap(kMode)>(p, taddr, row, tile, st);
 }
@@ -500,147 +571,6 @@ __device__ __forceinline__ void epilogue_unit(const Stage1Params& p, uint32_t ta
 template <int kMode>
 __device__ __forceinline__ void epilogue_finish(const Stage1Params& p, EpilogueState<kMode>& st) {
   if constexpr (kMode == kModeTop4 || kMode == kModeTop16) topk_flush<topk_cap(kMode)>(p, st);
-}
-
-// The last unit of a CTA in the sampling mode, when the batch has at most
-// kSpreadRows rows.  Nothing overlaps the epilogue of a CTA's last unit, and
-// with few rows only one or two lane quadrants hold rows, so only the two
-// warps of each such quadrant would work through 128 ids a row each.
-// Instead every epilogue warp copies its rows' logits out of tensor memory
-// into the (now idle) ring of shared memory, and the eight warps then take
-// one 32-id chunk of one row each (two with more than 32 rows); a second pass
-// merges each tile's four chunks in id order.  The per-chunk arithmetic is
-// the same as the other path's, so the samples and tile outputs are
-// bit-identical to it.
-constexpr int kSpreadRows = 64;
-constexpr uint32_t kSpreadRowBytes = kBlockN * 4 + 16;  // a row of fp32 logits + 16 B pad
-constexpr uint32_t kSpreadResOffset = kSpreadRows * kSpreadRowBytes;
-static_assert(kSpreadResOffset + kSpreadRows * 8 * 8 <= kRingBytes, "spread buffers fit the ring");
-
-struct ChunkBest {
-  float best;  // base-2 score (greedy rows: the logit)
-  int32_t j;   // its position in the chunk, -1 if none
-};
-
-__device__ __forceinline__ void spread_stage(uint8_t* smem, uint32_t taddr, int r, int col0) {
-  uint8_t* dst = smem + size_t(r) * kSpreadRowBytes + size_t(col0) * 4;
-#pragma unroll 1
-  for (int c = 0; c < kTileV / 32; ++c) {
-    uint32_t v[32];
-    ptx::tmem_ld_32x32b_x32(taddr + uint32_t(c * 32), v);
-    ptx::tmem_wait_ld();
-    uint4* d4 = reinterpret_cast<uint4*>(dst + c * 128);
-#pragma unroll
-    for (int q = 0; q < 8; ++q) d4[q] = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-  }
-}
-
-// One 32-id chunk (row r of the unit, ids vt*256 + 32c ..) from the staged
-// logits: its best score and position, as in epilogue_tile.  `valid` lanes
-// only; every lane of the warp takes part in the mask vote.
-__device__ __forceinline__ ChunkBest spread_chunk(const Stage1Params& p, const uint8_t* smem,
-                                                  int vt, int r, int c, bool valid) {
-  ChunkBest out{-INFINITY, -1};
-  const int v0 = vt * kBlockN + c * 32;
-  float T = 1.0f;
-  uint64_t seed = p.seed;
-  uint32_t allow = 0u;
-  if (valid) {
-    if (p.temperature) T = p.temperature[r];
-    if (p.seeds) seed = p.seeds[r];
-    allow = p.mask ? p.mask[int64_t(r) * p.mask_ld + (v0 >> 5)] : 0xFFFFFFFFu;
-    const int n_in = p.V - v0;
-    if (n_in < 32) allow &= (n_in <= 0) ? 0u : ((1u << n_in) - 1u);
-  }
-  const bool unmasked = __all_sync(0xFFFFFFFFu, allow == 0xFFFFFFFFu);
-  if (!valid) return out;
-  uint32_t v[32];
-  const uint4* s4 = reinterpret_cast<const uint4*>(smem + size_t(r) * kSpreadRowBytes + c * 128);
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    const uint4 x = s4[q];
-    v[4 * q] = x.x, v[4 * q + 1] = x.y, v[4 * q + 2] = x.z, v[4 * q + 3] = x.w;
-  }
-  const bool greedy = !(T > 0.0f) || isinf(T);
-  if (greedy) {
-    if (unmasked)
-      greedy_chunk<false>(v, allow, out.best, out.j);
-    else
-      greedy_chunk<true>(v, allow, out.best, out.j);
-  } else {
-    const float scale2 = kLog2e / T;
-    const PhiloxSchedule ks(seed);
-    const uint32_t ctr0 = static_cast<uint32_t>((p.vocab_offset + v0) >> 2);
-    const uint32_t ctr_row = static_cast<uint32_t>(r);
-    const uint32_t ctr_lo = static_cast<uint32_t>(p.offset);
-    const uint32_t ctr_hi = static_cast<uint32_t>(p.offset >> 32);
-    if (unmasked)
-      sample_chunk<false>(v, allow, scale2, ctr0, ctr_row, ctr_lo, ctr_hi, ks, out.best, out.j);
-    else
-      sample_chunk<true>(v, allow, scale2, ctr0, ctr_row, ctr_lo, ctr_hi, ks, out.best, out.j);
-  }
-  return out;
-}
-
-// The epilogue of the spread last unit, run by the eight epilogue warps once
-// the unit's accumulator is full.  Returns false if a wait timed out.
-__device__ __forceinline__ bool spread_last_unit(const Stage1Params& p, uint8_t* smem,
-                                                 uint32_t tmem_acc, int vt, int quad, int half,
-                                                 int lane, int e, const Waiter& waiter,
-                                                 uint64_t* staged_bar, uint64_t* chunks_bar) {
-  const int rows = p.B;  // one batch block of at most kSpreadRows rows
-  if (quad * 32 < rows)
-    spread_stage(smem, tmem_acc + (uint32_t(quad * 32) << 16) + uint32_t(half * kTileV),
-                 quad * 32 + lane, half * kTileV);
-  __syncwarp();
-  int ok = 1;
-  if (lane == 0) {
-    ptx::mbar_arrive(staged_bar);
-    ok = waiter.wait(staged_bar, 0) ? 1 : 0;
-  }
-  if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) return false;
-  // Chunk k: row (k % 32) + 32 (k / 256), chunk (k / 32) % 8, so the 32 lanes
-  // of a warp read 32 rows of one chunk (no shared-memory bank conflicts).
-  ChunkBest* res = reinterpret_cast<ChunkBest*>(smem + kSpreadResOffset);
-  const int n_items = ((rows + 31) / 32) * 32 * 8;
-  for (int k0 = e * 32; k0 < n_items; k0 += kEpiWarps * 32) {
-    const int k = k0 + lane;
-    const int r = (k & 31) + ((k >> 8) << 5), c = (k >> 5) & 7;
-    const bool valid = r < rows && vt * 2 + (c >> 2) < p.n_tiles;
-    const ChunkBest b = spread_chunk(p, smem, vt, r, c, valid);
-    if (valid) res[r * 8 + c] = b;
-  }
-  __syncwarp();
-  if (lane == 0) {
-    ptx::mbar_arrive(chunks_bar);
-    ok = waiter.wait(chunks_bar, 0) ? 1 : 0;
-  }
-  if (!__shfl_sync(0xFFFFFFFFu, ok, 0)) return false;
-  // Each (row, tile): its four chunks in id order, as epilogue_tile.
-  for (int k = e * 32 + lane; k < rows * 2; k += kEpiWarps * 32) {
-    const int r = k >> 1, h = k & 1, tile = vt * 2 + h;
-    if (tile >= p.n_tiles) continue;
-    const float T = p.temperature ? p.temperature[r] : 1.0f;
-    const bool greedy = !(T > 0.0f) || isinf(T);
-    float best = -INFINITY;
-    int32_t best_idx = -1;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const ChunkBest b = res[r * 8 + h * 4 + c];
-      if (b.j >= 0 && b.best > best) {
-        best = b.best;
-        best_idx = p.vocab_offset + tile * kTileV + c * 32 + b.j;
-      }
-    }
-    const float m = (greedy || best_idx < 0) ? best : kLn2 * (best - kLog2Ln2);
-    if (p.out_idx != nullptr && best_idx >= 0) atomicMax(p.row_keys + r, pack_key(m, best_idx));
-    if (p.tile_max != nullptr) {
-      const int64_t o = int64_t(r) * p.n_tiles + tile;
-      p.tile_max[o] = m;
-      p.tile_idx[o] = best_idx;
-    }
-  }
-  return true;
 }
 
 // Single-CTA stage 1: a unit is (vocabulary block vt of 256 ids, batch block mt
@@ -659,9 +589,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tfull_bar = empty_bar + kMaxStages;
   uint64_t* tempty_bar = tfull_bar + 2;
   uint64_t* drain_bar = tempty_bar + 2;
-  uint64_t* staged_bar = drain_bar + 1;  // the spread last unit (spread_last_unit)
-  uint64_t* chunks_bar = staged_bar + 1;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(chunks_bar + 1);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain_bar + 1);
   volatile uint32_t* abort_flag = tmem_holder + 1;
 
   const int warp = threadIdx.x >> 5;
@@ -679,8 +607,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(&tempty_bar[a], kEpiWarps);
     }
     ptx::mbar_init(drain_bar, 1);
-    ptx::mbar_init(staged_bar, kEpiWarps);
-    ptx::mbar_init(chunks_bar, kEpiWarps);
     *abort_flag = 0u;
     ptx::fence_barrier_init();
   }
@@ -834,24 +760,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     EpilogueState<kMode> est;
     for (int unit = blockIdx.x; unit < n_units; unit += gridDim.x) {
       const int vt = unit / p.n_mt, mt = unit % p.n_mt;
+      const int row0 = mt * kBlockM + quad * 32;
+      const int tile = vt * 2 + half;
+      const bool work = row0 < p.B && tile < p.n_tiles;
+      const bool last = unit + int(gridDim.x) >= n_units;
+      // This warp's lanes and columns of both accumulator buffers.
+      const uint32_t lanes = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(half * kTileV);
+      // A CTA's last unit in the sampling modes: its noise is made while its
+      // W slices stream in.  (The top-K modes make theirs in the epilogue:
+      // the noise beside their lists needed more registers than a thread has.)
+      const bool ahead = !kTopkMode<kMode> && last && work;
+      const uint32_t other = lanes + (acc ^ 1u) * kBlockN;
+      if (ahead) noise_ahead(p, other, row0 + lane, tile);
       int ok = 0;
       if (lane == 0) ok = waiter.wait(&tfull_bar[acc], acc_phase) ? 1 : 0;
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok) break;
       ptx::tc_fence_after();
-      if (kMode == kModeSample && p.B <= kSpreadRows && unit + int(gridDim.x) >= n_units) {
-        // The CTA's last unit, spread over all epilogue warps (then done).
-        spread_last_unit(p, smem, tmem_base + acc * kBlockN, vt, quad, half, lane, e, waiter,
-                         staged_bar, chunks_bar);
-        break;
-      }
-      const int row0 = mt * kBlockM + quad * 32;
-      const int tile = vt * 2 + half;
-      if (row0 < p.B && tile < p.n_tiles) {
-        const uint32_t taddr =
-            tmem_base + (uint32_t(quad * 32) << 16) + acc * kBlockN + uint32_t(half * kTileV);
-        epilogue_unit<kMode>(p, taddr, row0 + lane, tile, est);
-      }
+      if (ahead)
+        epilogue_unit<kMode, true>(p, lanes + acc * kBlockN, row0 + lane, tile, est, other);
+      else if (work)
+        epilogue_unit<kMode, false>(p, lanes + acc * kBlockN, row0 + lane, tile, est, 0u);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&tempty_bar[acc]);
@@ -1082,7 +1011,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (row0 < p.B && tile < p.n_tiles) {
         const uint32_t taddr =
             tmem_base + (uint32_t(quad * 32) << 16) + acc * kBlockN + uint32_t(half * kTileV);
-        epilogue_unit<kMode>(p, taddr, row0 + lane, tile, est);
+        epilogue_unit<kMode, false>(p, taddr, row0 + lane, tile, est, 0u);
       }
       ptx::tc_fence_before();
       __syncwarp();

@@ -173,12 +173,13 @@ def test_rows_do_not_depend_on_the_batch(V):
 
 
 @pytest.mark.parametrize("B", [1, 5, 32, 40, 64])
-def test_spread_last_unit_is_bit_identical(B):
-    """In the sampling mode, batches of at most 64 rows spread each CTA's last
-    unit over all epilogue warps (through shared memory); a batch of 128 rows
-    does not.  The same rows inside both must give bit-identical samples and
-    per-tile maxima and argmaxes (masks, greedy rows and per-row seeds
-    included), and both must match the oracle."""
+def test_partial_batch_block_is_bit_identical(B):
+    """A batch of fewer than 128 rows copies only its own H rows into each
+    stage (the MMA's other accumulator rows read whatever follows and are
+    never used), so fewer lane quadrants hold rows.  The same rows inside a
+    full 128-row block must give bit-identical samples and per-tile maxima and
+    argmaxes (masks, greedy rows and per-row seeds included), and both must
+    match the oracle."""
     big = make_problem(128, 264, 5000, T="row-uniform", per_row_seeds=True, mask_frac=0.05,
                        seed=120)
     ref = run_device(big, seed=9, offset=4, lse=False)
@@ -188,6 +189,29 @@ def test_spread_last_unit_is_bit_identical(B):
     for k in ("idx", "tile_max", "tile_idx"):
         assert np.array_equal(got[k], ref[k][:B]), k
     compare(sub, got, seed=9, offset=4, scores=True)
+
+
+@pytest.mark.parametrize("lse", [False, True])
+def test_noise_made_ahead_is_bit_identical(lse):
+    """In the single-CTA kernel each CTA's last unit reads noise that its
+    epilogue warps wrote into tensor memory while the unit's W slices streamed
+    in; every other unit (and every unit of the CTA-pair kernel) makes its
+    noise in the epilogue.  Which units are last depends on the batch: at
+    B = 128 the last wave covers other vocabulary blocks than at B = 384
+    (three batch blocks), and B = 256 runs on CTA pairs.  The same rows must
+    give bit-identical samples and tile outputs (greedy rows, masks and
+    per-row seeds included) and match the oracle."""
+    V = 151936
+    big = make_problem(384, 128, V, T="row-uniform", per_row_seeds=True, mask_frac=0.05,
+                       seed=121)
+    ref = run_device(big, seed=3, offset=8, lse=lse)
+    for B in (128, 256):
+        sub = {k: (None if t is None else t[:B].contiguous()) if k != "W" else t
+               for k, t in big.items()}
+        got = run_device(sub, seed=3, offset=8, lse=lse)
+        for k in got:
+            assert np.array_equal(got[k], ref[k][:B]), (B, k)
+    compare(sub, got, rows=[0, 77, 128, 200, 255], seed=3, offset=8)
 
 
 def test_tiny_temperature_is_effectively_greedy():
