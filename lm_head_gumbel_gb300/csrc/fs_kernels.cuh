@@ -433,7 +433,8 @@ __device__ __forceinline__ void topk_flush(const Stage1Params& p, const TopKStat
 // per id that any lane wants.
 template <int KC>
 __device__ __forceinline__ void epilogue_tile_topk(const Stage1Params& p, uint32_t taddr,
-                                                   int row, int tile, TopKState<KC>& st) {
+                                                   int row, int tile, TopKState<KC>& st,
+                                                   uint32_t ntaddr, bool pre) {
   const bool valid_row = row < p.B;
   float T = 1.0f;
   uint64_t seed = p.seed;
@@ -451,9 +452,14 @@ __device__ __forceinline__ void epilogue_tile_topk(const Stage1Params& p, uint32
       }
       st.row = row;
     }
-    const int64_t o = (int64_t(row) * p.n_tiles + tile) * KC;
-    p.topk_score[o] = -INFINITY;  // empty unless the stretch's list lands here
-    p.topk_idx[o] = -1;
+    // The slot is empty unless the stretch's list lands here.  Its first id
+    // alone marks it, but written as whole 32-byte sectors (16 bytes at
+    // KC = 4, whose neighbour tile writes the other half at about the same
+    // time): a partly written sector is read back from DRAM when it leaves
+    // the L2, beside the W stream.
+    int4* m4 = reinterpret_cast<int4*>(p.topk_idx + (int64_t(row) * p.n_tiles + tile) * KC);
+    m4[0] = make_int4(-1, -1, -1, -1);
+    if (KC >= 8) m4[1] = make_int4(-1, -1, -1, -1);
     st.last_tile = tile;
   }
   const bool greedy = !(T > 0.0f) || isinf(T);
@@ -463,15 +469,19 @@ __device__ __forceinline__ void epilogue_tile_topk(const Stage1Params& p, uint32
   const uint32_t ctr_row = static_cast<uint32_t>(row);
   const uint32_t ctr_lo = static_cast<uint32_t>(p.offset);
   const uint32_t ctr_hi = static_cast<uint32_t>(p.offset >> 32);
+  // noise_ahead wrote noise only for warps with a sampled row.
+  const bool load_noise = pre && __any_sync(0xFFFFFFFFu, valid_row && !greedy);
   const int v_tile = tile * kTileV;
 #pragma unroll 1
   for (int c = 0; c < kTileV / 32; ++c) {
     uint32_t r[32];
+    float sc[32];
     ptx::tmem_ld_32x32b_x32(taddr + uint32_t(c * 32), r);
+    if (load_noise)  // the noise lands in sc; the scores are made in place below
+      ptx::tmem_ld_32x32b_x32(ntaddr + uint32_t(c * 32), reinterpret_cast<uint32_t(&)[32]>(sc));
     ptx::tmem_wait_ld();
     const int v0 = v_tile + c * 32;
     const int32_t id0 = p.vocab_offset + v0;
-    float sc[32];
     uint32_t cand = 0u;
     if (valid_row) {
       uint32_t allow = mrow ? mrow[v0 >> 5] : 0xFFFFFFFFu;
@@ -480,6 +490,9 @@ __device__ __forceinline__ void epilogue_tile_topk(const Stage1Params& p, uint32
       if (greedy) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) sc[j] = __uint_as_float(r[j]);
+      } else if (pre) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) sc[j] = fmaf(__uint_as_float(r[j]), scale2, -sc[j]);
       } else {
 #pragma unroll
         for (int g = 0; g < 8; ++g) {
@@ -554,17 +567,23 @@ using EpilogueState =
     typename std::conditional<(kMode == kModeTop4 || kMode == kModeTop16),
                               TopKState<topk_cap(kMode)>, NoState>::type;
 
-// One unit's epilogue for one thread; with kPreNoise (sampling modes only)
-// the noise is read from tensor memory at ntaddr (noise_ahead) instead of
-// being made.
-template <int kMode, bool kPreNoise>
+// One unit's epilogue for one thread.  With `pre` the noise is read from
+// tensor memory at ntaddr (noise_ahead) instead of being made.  The sampling
+// modes inline a form of each; the top-K modes test the flag inside one form
+// (two inlined forms beside the lists needed more registers than a thread
+// has, and spilled).
+template <int kMode>
 __device__ __forceinline__ void epilogue_unit(const Stage1Params& p, uint32_t taddr, int row,
                                               int tile, EpilogueState<kMode>& st,
-                                              uint32_t ntaddr) {
-  if constexpr (kMode == kModeSample || kMode == kModeLse)
-    epilogue_tile<kMode == kModeLse, kPreNoise>(p, taddr, row, tile, ntaddr);
-  else
-    epilogue_tile_topk<topk_cap(kMode)>(p, taddr, row, tile, st);
+                                              uint32_t ntaddr, bool pre) {
+  if constexpr (kMode == kModeSample || kMode == kModeLse) {
+    if (pre)
+      epilogue_tile<kMode == kModeLse, true>(p, taddr, row, tile, ntaddr);
+    else
+      epilogue_tile<kMode == kModeLse, false>(p, taddr, row, tile, 0u);
+  } else {
+    epilogue_tile_topk<topk_cap(kMode)>(p, taddr, row, tile, st, ntaddr, pre);
+  }
 }
 
 // After a thread's last unit: the top-K modes write the open stretch's list.
@@ -766,10 +785,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool last = unit + int(gridDim.x) >= n_units;
       // This warp's lanes and columns of both accumulator buffers.
       const uint32_t lanes = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(half * kTileV);
-      // A CTA's last unit in the sampling modes: its noise is made while its
-      // W slices stream in.  (The top-K modes make theirs in the epilogue:
-      // the noise beside their lists needed more registers than a thread has.)
-      const bool ahead = !kTopkMode<kMode> && last && work;
+      // A CTA's last unit: its noise is made while its W slices stream in.
+      const bool ahead = last && work;
       const uint32_t other = lanes + (acc ^ 1u) * kBlockN;
       if (ahead) noise_ahead(p, other, row0 + lane, tile);
       int ok = 0;
@@ -777,10 +794,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok) break;
       ptx::tc_fence_after();
-      if (ahead)
-        epilogue_unit<kMode, true>(p, lanes + acc * kBlockN, row0 + lane, tile, est, other);
-      else if (work)
-        epilogue_unit<kMode, false>(p, lanes + acc * kBlockN, row0 + lane, tile, est, 0u);
+      if (work)
+        epilogue_unit<kMode>(p, lanes + acc * kBlockN, row0 + lane, tile, est, other, ahead);
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&tempty_bar[acc]);
@@ -1011,7 +1026,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (row0 < p.B && tile < p.n_tiles) {
         const uint32_t taddr =
             tmem_base + (uint32_t(quad * 32) << 16) + acc * kBlockN + uint32_t(half * kTileV);
-        epilogue_unit<kMode, false>(p, taddr, row0 + lane, tile, est, 0u);
+        epilogue_unit<kMode>(p, taddr, row0 + lane, tile, est, 0u, false);
       }
       ptx::tc_fence_before();
       __syncwarp();

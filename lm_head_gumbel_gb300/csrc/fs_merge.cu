@@ -152,6 +152,15 @@ __device__ __forceinline__ bool precedes(float as, int32_t ai, float bs, int32_t
 
 constexpr int kTopkThreads = 256;
 
+// An order-preserving map of non-NaN floats to unsigned integers, and back.
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_score(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
 // Merge a sorted list c into the sorted list l, keeping the KC best: the
 // better of l[q] and c[KC-1-q] for every q is a bitonic sequence holding the
 // KC best of both, which a bitonic merge network sorts.
@@ -323,9 +332,6 @@ __global__ void __launch_bounds__(kTopkThreads)
   constexpr int kWarps = kTopkThreads / 32;
   __shared__ float s_part[kWarps];
   __shared__ int s_n;
-  __shared__ float s_tau_head;
-  __shared__ float s_hs[kTopkThreads];
-  __shared__ int32_t s_hi[kTopkThreads];
   __shared__ float s_score[kSurvivorCap];
   __shared__ int32_t s_id[kSurvivorCap];
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the stage-1 grid is complete
@@ -334,7 +340,6 @@ __global__ void __launch_bounds__(kTopkThreads)
   const int64_t base = int64_t(row) * n_tiles * KC;
   if (threadIdx.x == 0) {
     s_n = 0;
-    s_tau_head = -INFINITY;
   }
   __syncthreads();
   // Each thread's best list head, and the largest K-th entry of a list: the
@@ -387,38 +392,21 @@ __global__ void __launch_bounds__(kTopkThreads)
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) tau = fmaxf(tau, __shfl_xor_sync(0xFFFFFFFFu, tau, off));
   if (lane == 0) s_part[warp] = tau;
-  // Sort the threads' best heads, best first (bitonic network: exchanges
-  // within a warp by shuffles, across warps through shared memory); the K-th
-  // of them is reached by K distinct entries.
-#pragma unroll
-  for (int k = 2; k <= kTopkThreads; k <<= 1) {
-#pragma unroll
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      float os;
-      int32_t oi;
-      if (j >= 32) {
-        __syncthreads();
-        s_hs[threadIdx.x] = hb;
-        s_hi[threadIdx.x] = hbi;
-        __syncthreads();
-        os = s_hs[threadIdx.x ^ j];
-        oi = s_hi[threadIdx.x ^ j];
-      } else {
-        os = __shfl_xor_sync(0xFFFFFFFFu, hb, j);
-        oi = __shfl_xor_sync(0xFFFFFFFFu, hbi, j);
-      }
-      const bool lower = (threadIdx.x & j) == 0;
-      const bool best_first = (threadIdx.x & k) == 0;
-      const bool other_better = precedes(os, oi, hb, hbi);
-      if (other_better == (lower == best_first)) {
-        hb = os;
-        hbi = oi;
-      }
-    }
+  // The largest score that at least K of the threads' best heads reach (K
+  // distinct entries reach it), by bisection over the order-preserving
+  // integer image of the scores, one block-wide count per step.  It stops
+  // when the interval is 2^11 images wide (a relative width of about 2^-12):
+  // its lower end still has K heads reaching it and lets few more entries by.
+  const uint32_t my = hbi >= 0 ? order_key(hb) : 0u;  // no head: below every score
+  uint32_t lo = 0u, hi = 0xFFFFFFFFu;
+  while (hi - lo > (1u << 11)) {
+    const uint32_t mid = lo + ((hi - lo) >> 1) + 1u;
+    if (__syncthreads_count(my >= mid) >= K)
+      lo = mid;
+    else
+      hi = mid - 1u;
   }
-  if (threadIdx.x == K - 1) s_tau_head = hbi >= 0 ? hb : -INFINITY;
-  __syncthreads();
-  tau = s_tau_head;
+  tau = lo <= order_key(-INFINITY) ? -INFINITY : key_score(lo);
 #pragma unroll
   for (int w = 0; w < kWarps; ++w) tau = fmaxf(tau, s_part[w]);
   // The entries reaching tau, from the lists whose head reaches it (the heads
