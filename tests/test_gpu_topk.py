@@ -185,6 +185,27 @@ def test_topk_full_size_head(B, K):
     assert check_against_oracle(p, K, idx, score, rows=rows, offset=2) >= len(rows) * K * 0.6
 
 
+@pytest.mark.parametrize("name,B,K", [("qwen3-8b", 64, 16), ("qwen3-1.7b", 256, 4)])
+def test_topk_whole_batch_against_oracle(name, B, K):
+    """Every row of a production-shaped batch against the oracle's fp64
+    top-K (gap-gated): the Qwen3-8B head at the benchmark's top-K leg (B = 64,
+    K = 16, the single-CTA kernel, whose last units read their noise made
+    ahead) and the Qwen3-1.7B head at B = 256 (the CTA-pair kernel); every
+    row's first id against fs_sample."""
+    w = wl.WORKLOADS[name]
+    W = wl.make_weights(w.d, w.V, seed=77, device="cuda")
+    p = make_problem(B, w.d, w.V, T="row-uniform", per_row_seeds=True, seed=160 + B, W=W)
+    idx, score = device_topk(p, K, offset=9)
+    one = fs.fs_sample(p["H"], W, temperature=p["temperature"], seeds=p["seeds"], offset=9,
+                       seed=7)
+    torch.cuda.synchronize()
+    assert np.array_equal(idx[:, 0], one.cpu().numpy())
+    for b in range(B):
+        assert len(set(idx[b].tolist())) == K, b
+    n_exact = check_against_oracle(p, K, idx, score, rows=list(range(B)), offset=9)
+    assert n_exact >= B * K * 0.6
+
+
 @pytest.mark.parametrize("K", [4, 16])
 def test_topk_equal_scores_take_the_lowest_ids(K):
     """Every logit of a row equal (all W rows the same): greedy rows tie on
