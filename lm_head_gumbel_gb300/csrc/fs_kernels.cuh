@@ -413,11 +413,17 @@ template <int KC>
 __device__ __forceinline__ void topk_flush(const Stage1Params& p, const TopKState<KC>& st) {
   if (st.row < 0) return;
   const int64_t o = (int64_t(st.row) * p.n_tiles + st.last_tile) * KC;
+  // The slot is KC contiguous scores then (elsewhere) KC ids, 16-byte aligned.
+  float4* s4 = reinterpret_cast<float4*>(p.topk_score + o);
+  int4* i4 = reinterpret_cast<int4*>(p.topk_idx + o);
 #pragma unroll
-  for (int q = 0; q < KC; ++q) {
-    const float m = (st.greedy || st.i[q] < 0) ? st.s[q] : kLn2 * (st.s[q] - kLog2Ln2);
-    p.topk_score[o + q] = m;
-    p.topk_idx[o + q] = st.i[q];
+  for (int q = 0; q < KC; q += 4) {
+    float m[4];
+#pragma unroll
+    for (int x = 0; x < 4; ++x)
+      m[x] = (st.greedy || st.i[q + x] < 0) ? st.s[q + x] : kLn2 * (st.s[q + x] - kLog2Ln2);
+    s4[q / 4] = make_float4(m[0], m[1], m[2], m[3]);
+    i4[q / 4] = make_int4(st.i[q], st.i[q + 1], st.i[q + 2], st.i[q + 3]);
   }
 }
 
