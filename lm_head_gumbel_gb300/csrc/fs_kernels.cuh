@@ -261,6 +261,29 @@ __device__ __forceinline__ void noise_ahead(const Stage1Params& p, uint32_t ntad
   ptx::tmem_wait_st();
 }
 
+// The allow-words of one row's 128-id tile, all loaded before the tile's
+// chunks are processed (a word loaded inside the chunk loop would be waited
+// for after each chunk's tensor-memory load).  Only words holding ids below V
+// are read -- the ceil(V/32) words a mask row has -- and ids at or past V are
+// allowed nowhere.
+struct TileMask {
+  uint32_t w[kTileV / 32];
+  __device__ __forceinline__ TileMask(const uint32_t* mrow, int v_tile, int V) {
+#pragma unroll
+    for (int c = 0; c < kTileV / 32; ++c) {
+      const int v0 = v_tile + c * 32;
+      const int n_in = V - v0;
+      w[c] = n_in <= 0 ? 0u : (mrow != nullptr ? mrow[v0 >> 5] : 0xFFFFFFFFu);
+      if (n_in > 0 && n_in < 32) w[c] &= (1u << n_in) - 1u;
+    }
+  }
+  // Word c, for a chunk index known only at run time, without local memory.
+  __device__ __forceinline__ uint32_t at(int c) const {
+    return c == 0 ? w[0] : c == 1 ? w[1] : c == 2 ? w[2] : w[3];
+  }
+};
+static_assert(kTileV / 32 == 4, "TileMask::at picks one of four words");
+
 // One thread, one batch row, one 128-id output tile: read the logits from
 // tensor memory 32 columns at a time and reduce them to (m_t, i_t[, L_t]).
 // With kPreNoise the noise is read from tensor memory at ntaddr (noise_ahead)
@@ -290,6 +313,7 @@ __device__ __forceinline__ void epilogue_tile(const Stage1Params& p, uint32_t ta
   int32_t best_idx = -1;
   float run_max = -INFINITY, run_sum = 0.0f;  // base-2 log-sum-exp state
   const int v_tile = tile * kTileV;
+  const TileMask tm(mrow, v_tile, p.V);  // mrow is null for rows past the batch
 
 #pragma unroll 1
   for (int c = 0; c < kTileV / 32; ++c) {
@@ -299,12 +323,7 @@ __device__ __forceinline__ void epilogue_tile(const Stage1Params& p, uint32_t ta
     if (load_noise) ptx::tmem_ld_32x32b_x32(ntaddr + uint32_t(c * 32), qn);
     ptx::tmem_wait_ld();
     const int v0 = v_tile + c * 32;
-    uint32_t allow = 0xFFFFFFFFu;
-    if (valid_row) {
-      if (mrow) allow = mrow[v0 >> 5];
-      const int n_in = p.V - v0;
-      if (n_in < 32) allow &= (n_in <= 0) ? 0u : ((1u << n_in) - 1u);
-    }
+    const uint32_t allow = valid_row ? tm.at(c) : 0xFFFFFFFFu;
     // The mask test is skipped only when no lane of the warp needs it: a
     // per-lane choice would run both forms one after the other.
     const bool unmasked = __all_sync(0xFFFFFFFFu, allow == 0xFFFFFFFFu);
@@ -478,6 +497,7 @@ __device__ __forceinline__ void epilogue_tile_topk(const Stage1Params& p, uint32
   // noise_ahead wrote noise only for warps with a sampled row.
   const bool load_noise = pre && __any_sync(0xFFFFFFFFu, valid_row && !greedy);
   const int v_tile = tile * kTileV;
+  const TileMask tm(mrow, v_tile, p.V);  // mrow is null for rows past the batch
 #pragma unroll 1
   for (int c = 0; c < kTileV / 32; ++c) {
     uint32_t r[32];
@@ -490,9 +510,7 @@ __device__ __forceinline__ void epilogue_tile_topk(const Stage1Params& p, uint32
     const int32_t id0 = p.vocab_offset + v0;
     uint32_t cand = 0u;
     if (valid_row) {
-      uint32_t allow = mrow ? mrow[v0 >> 5] : 0xFFFFFFFFu;
-      const int n_in = p.V - v0;
-      if (n_in < 32) allow &= (n_in <= 0) ? 0u : ((1u << n_in) - 1u);
+      const uint32_t allow = tm.at(c);
       if (greedy) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) sc[j] = __uint_as_float(r[j]);
