@@ -99,6 +99,10 @@ struct Stage1Params {
   // (programmatic dependent launch): W streams at once, H and the per-row
   // inputs are read only after the grid dependency is resolved.
   uint32_t pdl;
+  // CTA-pair kernel with more than one pair batch block: groups of pairs
+  // walking the same vocabulary blocks (pair_unit); 0 for the plain order.
+  int32_t pair_groups;        // groups of n_mp pairs
+  int32_t pair_group_blocks;  // vocabulary blocks each group walks
 };
 
 // The producer's H copies of the first ring fill, held back until the grid
@@ -861,7 +865,42 @@ constexpr size_t kPairSmemBytes = 1024 + kPairBarOffset + 256;
 constexpr uint32_t kPairIdesc = ptx::idesc_bf16_f32(2 * kBlockM, kBlockN);
 static_assert(kPairSmemBytes <= 232448, "pair kernel shared memory");
 
-template <int kMode>
+// The unit (vocabulary block vt, pair batch block mp) that CTA pair `pair`
+// takes k-th; false when it has no more.  Plain order: unit pair + k * n_pairs
+// of the vocabulary-major list, so the n_mp units of one vocabulary block run
+// on neighbouring pairs at about the same time and all but the first read its
+// W tile from L2; a pair's batch block changes from one unit to the next
+// unless n_pairs is a multiple of n_mp.  Grouped order (kGrouped, launched by
+// the host for the top-K modes when it needs no more waves than the plain
+// one): groups of n_mp pairs walk the same vocabulary blocks, pair j of a
+// group always on batch block j, so each of its epilogue threads keeps one row
+// for the whole call -- one candidate list a thread instead of one a unit;
+// the pairs left over take the remaining blocks whole, one batch block after
+// the other.  (A separate kernel: the grouped loop in the plain kernels cost
+// the sampling modes about 0.5 % and spilled the top-K modes' registers.)
+template <bool kGrouped>
+__device__ __forceinline__ bool pair_unit(const Stage1Params& p, int pair, int k, int n_pairs,
+                                          int n_mp, int n_vt, int& vt, int& mp) {
+  if constexpr (kGrouped) {
+    const int G = p.pair_groups;
+    if (pair < G * n_mp) {
+      vt = pair / n_mp + k * G;
+      mp = pair % n_mp;
+      return k < p.pair_group_blocks && vt < n_vt;
+    }
+    const int n_left = n_pairs - G * n_mp, l = pair - G * n_mp;
+    vt = min(n_vt, G * p.pair_group_blocks) + l + (k / n_mp) * n_left;
+    mp = k % n_mp;
+    return vt < n_vt;
+  } else {
+    const int u = pair + k * n_pairs;
+    vt = u / n_mp;
+    mp = u % n_mp;
+    return u < n_vt * n_mp;
+  }
+}
+
+template <int kMode, bool kGrouped>
 __global__ void __launch_bounds__(kThreads, 1)
     stage1_pair_kernel(const __grid_constant__ CUtensorMap tmap_h,
                        const __grid_constant__ CUtensorMap tmap_w, const Stage1Params p) {
@@ -883,7 +922,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int pair_id = int(blockIdx.x) >> 1;
   const int n_pairs = int(gridDim.x) >> 1;
   const int n_mp = (p.B + 2 * kBlockM - 1) / (2 * kBlockM);
-  const int n_units = ((p.n_tiles + 1) / 2) * n_mp;  // not from V + 255 (32-bit overflow)
+  const int n_vt = (p.n_tiles + 1) / 2;  // not from V + 255 (32-bit overflow)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kPairStages; ++s) {
@@ -935,8 +974,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         defer.n = 0;
         deferring = false;
       };
-      for (int u = pair_id; ok && u < n_units; u += n_pairs) {
-        const int vt = u / n_mp, mp = u % n_mp;
+      int vt, mp;
+      for (int k = 0;
+           ok && pair_unit<kGrouped>(p, pair_id, k, n_pairs, n_mp, n_vt, vt, mp); ++k) {
         const int k_start =
             int((uint32_t(vt + (p.vocab_offset >> 8)) * 5u) % uint32_t(p.n_kb));
         // Rows past the end are read from the last valid row instead (their
@@ -992,7 +1032,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t s0 = ptx::smem_u32(smem);
       const uint64_t desc_a0 = ptx::smem_desc_sw128(s0);
       const uint64_t desc_b0 = ptx::smem_desc_sw128(s0 + kPairSmemA);
-      for (int u = pair_id; ok && u < n_units; u += n_pairs) {
+      int vt, mp;
+      for (int k = 0;
+           ok && pair_unit<kGrouped>(p, pair_id, k, n_pairs, n_mp, n_vt, vt, mp); ++k) {
         if (!waiter.wait_warp(&tempty_bar[acc], acc_phase ^ 1u)) break;
         ptx::tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * kBlockN;
@@ -1038,8 +1080,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tempty_addr1 = ptx::cluster_addr(&tempty_bar[1], 0);
     uint32_t acc = 0, acc_phase = 0;
     EpilogueState<kMode> est;
-    for (int u = pair_id; u < n_units; u += n_pairs) {
-      const int vt = u / n_mp, mp = u % n_mp;
+    int vt, mp;
+    for (int k = 0; pair_unit<kGrouped>(p, pair_id, k, n_pairs, n_mp, n_vt, vt, mp); ++k) {
       int ok = 0;
       if (lane == 0) ok = waiter.wait(&tfull_bar[acc], acc_phase) ? 1 : 0;
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);

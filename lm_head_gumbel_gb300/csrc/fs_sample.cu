@@ -6,6 +6,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <algorithm>
 #include <atomic>
 #include <chrono>
 #include <climits>
@@ -76,10 +77,16 @@ bool prepare_mode(DeviceState& st, int sms) {
   if (cudaFuncSetAttribute(stage1_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            int(kSmemBytes)) != cudaSuccess)
     return false;
-  auto pk = stage1_pair_kernel<kMode>;
+  auto pk = stage1_pair_kernel<kMode, false>;
   if (cudaFuncSetAttribute(pk, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            int(kPairSmemBytes)) != cudaSuccess)
     return false;
+  if constexpr (kTopkMode<kMode>) {  // the grouped unit order (same resources)
+    if (cudaFuncSetAttribute(stage1_pair_kernel<kMode, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(kPairSmemBytes)) != cudaSuccess)
+      return false;
+  }
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = launch_config(2, attr, nullptr, kPairSmemBytes);
   cfg.gridDim = dim3(unsigned((sms / 2) * 2), 1, 1);
@@ -108,11 +115,33 @@ fs_status launch_mode(bool pair, const CUtensorMap& tmap_h, const CUtensorMap& t
   cudaLaunchAttribute attr[2];
   cudaError_t err;
   if (pair) {
-    const int n_units = n_vt * int((int64_t(p.B) + 2 * kBlockM - 1) / (2 * kBlockM));
+    const int n_mp = int((int64_t(p.B) + 2 * kBlockM - 1) / (2 * kBlockM));
+    const int n_units = n_vt * n_mp;
     const int pairs = balanced_grid(n_units, ds.max_pairs[kMode]);
+    // The top-K modes' grouped unit order (pair_unit in fs_kernels.cuh) when
+    // it needs no more waves than the plain one: groups of n_mp pairs walk
+    // `waves` vocabulary blocks each, and the pairs left over take the rest.
+    Stage1Params q = p;
+    if (kTopkMode<kMode> && n_mp > 1) {
+      const int waves = (n_units + pairs - 1) / pairs;
+      const int groups = pairs / n_mp, n_left = pairs - groups * n_mp;
+      const int left = n_vt - std::min(n_vt, groups * waves);
+      if (groups > 0 &&
+          (left == 0 || (n_left > 0 && ((left + n_left - 1) / n_left) * n_mp <= waves))) {
+        q.pair_groups = groups;
+        q.pair_group_blocks = waves;
+      }
+    }
     cudaLaunchConfig_t cfg = launch_config(2, attr, stream, kPairSmemBytes, p.pdl != 0);
     cfg.gridDim = dim3(unsigned(pairs * 2), 1, 1);
-    err = cudaLaunchKernelEx(&cfg, stage1_pair_kernel<kMode>, tmap_h, tmap_w, p);
+    if constexpr (kTopkMode<kMode>) {
+      if (q.pair_groups > 0)
+        err = cudaLaunchKernelEx(&cfg, stage1_pair_kernel<kMode, true>, tmap_h, tmap_w, q);
+      else
+        err = cudaLaunchKernelEx(&cfg, stage1_pair_kernel<kMode, false>, tmap_h, tmap_w, q);
+    } else {
+      err = cudaLaunchKernelEx(&cfg, stage1_pair_kernel<kMode, false>, tmap_h, tmap_w, q);
+    }
   } else {
     const int n_units = n_vt * p.n_mt;
     const int grid = balanced_grid(n_units, ds.num_sms);
