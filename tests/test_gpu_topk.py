@@ -145,13 +145,17 @@ def test_topk_on_a_vocabulary_shard():
                 assert idx[b, j] == v0 + ridx[b, j], (b, j)
 
 
-@pytest.mark.parametrize("B,V", [(384, 5000), (512, 3000), (136, 40000)])
+@pytest.mark.parametrize("B,V", [(384, 5000), (512, 3000), (136, 40000), (1024, 40000)])
 def test_topk_rows_changing_between_units(B, V):
     """Batches whose epilogue threads change rows from unit to unit (three
-    128-row blocks on single CTAs; two 256-row pair blocks) or run long
-    stretches of one row (136 rows, 313 tiles): the running per-thread lists
-    are flushed at every row change; every row's first id is fs_sample's and
-    sampled rows match the oracle."""
+    128-row blocks on single CTAs) or run long stretches of one row (136
+    rows, 313 tiles; and the CTA pairs' grouped order, where a pair keeps one
+    batch block: two pair blocks of one unit a pair, and four pair blocks over
+    157 vocabulary blocks -- groups walking 9 blocks each plus leftover pairs
+    taking the last blocks one batch block after the other): the running
+    per-thread lists are flushed at every row change; every row's first id is
+    fs_sample's, no row repeats an id, and sampled rows of every batch block
+    match the oracle."""
     K = 16
     p = make_problem(B, 64, V, T="row-uniform", per_row_seeds=True, seed=60 + B)
     idx, score = device_topk(p, K, offset=4)
@@ -163,7 +167,7 @@ def test_topk_rows_changing_between_units(B, V):
     for b in range(B):
         got = idx[b][idx[b] >= 0]
         assert len(set(got.tolist())) == len(got) == K
-    rows = sorted({r for r in (0, 127, 128, 255, 256, B - 1) if r < B})
+    rows = sorted({r for r in (0, 127, 128, 255, 256, 511, 512, 767, 768, B - 1) if r < B})
     assert check_against_oracle(p, K, idx, score, rows=rows, offset=4) >= len(rows) * K * 0.7
 
 
