@@ -171,10 +171,12 @@ def test_topk_rows_changing_between_units(B, V):
     assert check_against_oracle(p, K, idx, score, rows=rows, offset=4) >= len(rows) * K * 0.7
 
 
-@pytest.mark.parametrize("B,K", [(64, 8), (256, 16)])
+@pytest.mark.parametrize("B,K", [(64, 8), (256, 16), (512, 16)])
 def test_topk_full_size_head(B, K):
     """Qwen3-8B-shaped head (d=4096, V=151936): the single-CTA kernel (B=64)
-    and the CTA-pair kernel (B=256) in top-K mode; sampled rows against the
+    and the CTA-pair kernel in top-K mode (B=256; B=512 in the grouped order:
+    37 groups of two pairs walk 16 vocabulary blocks each and the pair left
+    over takes the last two, both batch blocks); sampled rows against the
     oracle, every row's first id against fs_sample."""
     w = wl.WORKLOADS["qwen3-8b"]
     W = wl.make_weights(w.d, w.V, seed=77, device="cuda")
@@ -185,6 +187,8 @@ def test_topk_full_size_head(B, K):
     torch.cuda.synchronize()
     assert np.array_equal(idx[:, 0], one.cpu().numpy())
     assert np.all((idx >= 0) & (idx < w.V))
+    for b in range(B):
+        assert len(set(idx[b].tolist())) == K, b
     rows = [0, B // 3, B - 1]
     assert check_against_oracle(p, K, idx, score, rows=rows, offset=2) >= len(rows) * K * 0.6
 
