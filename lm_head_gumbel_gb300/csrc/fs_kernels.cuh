@@ -23,7 +23,10 @@
 //             columns (one output tile); it reads its logits from tensor
 //             memory, scales by 1/T, masks, adds Philox Gumbel noise, and
 //             keeps the running (max, argmax) and optionally the log-sum-exp
-//             -- or, in the top-K modes, the best 4 or 16 (score, id)
+//             -- or, in the top-K modes, the best 4 or 16 (score, id).  For a
+//             CTA's last unit the noise is made while its W streams in and
+//             parked in the idle accumulator (noise_ahead), since nothing
+//             overlaps that unit's epilogue
 // Only (m_t, i_t[, L_t]) -- or the top-K list -- per (row, 128-id tile)
 // leaves the chip.
 //
@@ -845,13 +848,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// Stage 1 for batches of more than 128 rows: CTA pairs (2-CTA clusters) run
-// M = 256, N = 256, K = 16 MMAs (cta_group::2).  A unit is (vocabulary block vt
+// Stage 1 for an even number of 128-row batch blocks: CTA pairs (2-CTA
+// clusters) run M = 256, N = 256, K = 16 MMAs (cta_group::2).  A unit is (vocabulary block vt
 // of 256 ids, pair block mp of 256 batch rows).  CTA r of the pair loads batch
 // rows mp*256 + r*128 .. +127 (its half of A) and vocabulary rows vt*256 +
 // r*128 .. +127 (its half of B) into its own shared memory, 32 KB a stage, so
 // six stages fit; every copy signals the even ("leader") CTA's full barrier.
-// The leader's single MMA thread accumulates into both CTAs' tensor memory
+// The leader's MMA warp (one elected lane) accumulates into both CTAs' tensor memory
 // (rows r*128.. in CTA r, all 256 columns) and multicasts its commits to both
 // CTAs' barriers.  Each CTA's epilogue reads its own 128 rows; the leader's
 // "tensor memory empty" barrier collects the epilogue warps of both CTAs.
