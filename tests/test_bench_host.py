@@ -113,3 +113,25 @@ def test_default_run_times_every_workload():
         assert ("fits in L2" in note) == (w.V * w.d * 2 <= bench.L2_BYTES)
     assert "fits in L2" in bench.l2_note(4096, 256)       # the tiny head: warm
     assert "exceed L2" in bench.l2_note(151936, 4096)     # the Qwen3-8B head: cold
+
+
+def test_traffic_record_covers_every_timed_point():
+    """The committed DRAM-traffic record has an entry for every (workload,
+    batch) the default run times -- the headline head's sweep and every other
+    workload's batches -- each a plausible multiple of the point's algorithmic
+    bytes.  (Whether it was taken on the current kernel source is decided at
+    run time: an older record yields `traffic: null`.)"""
+    import os
+    from lm_head_gumbel_gb300 import workloads as wl
+    with open(os.path.join(bench.ROOT, "profiles", "stage1_traffic.json")) as f:
+        rec = json.load(f)
+    launches = rec["launches"]
+    for name in bench.OTHER_WORKLOADS:
+        w = wl.WORKLOADS[name]
+        for B in w.batches:
+            ent = launches.get(f"{name}/B={B}")
+            assert ent is not None, (name, B)
+            algo, _flops = bench.algorithmic(B, w.d, w.V, seeds=w.per_row_seeds,
+                                             mask=bool(w.mask_frac), tiles=w.want_lse)
+            assert 0.95 * algo <= ent["dram_bytes_per_launch"] <= 2.0 * algo, (name, B)
+
